@@ -1,0 +1,607 @@
+"""Benchmark of the paged-KV attention hot path on GB300.
+
+One step = one decode step of a Qwen3-0.6B-shaped model at c=64 over its 28
+attention layers: for every layer, the KV store of the 64 new tokens (one per
+sequence, position 639) into that layer's paged cache, then paged decode
+attention of the 64 sequences at context 640 (16 query heads, 8 KV heads,
+head_dim 128, block size 256). Every layer has its own seeded cache (168 MB of
+K/V per layer, 4.7 GB per step, far larger than the 129 MB L2), so nothing is
+reused from L2 between layers or steps. The headline value is seq*layer/s.
+
+The same JSON line also carries:
+  roofline      the decode call (split + merge kernels) as the dominant kernel:
+                algorithmic bytes per call / CUDA-event duration per call,
+                against the measured HBM copy bandwidth;
+  prefill       the prefix-cached prefill (8 x 4096 new tokens over a shared
+                4096-token cached prefix, 1.649 TFLOP per call) in TFLOP/s,
+                against the measured bf16 tensor peak; and the KV store of
+                those 32768 tokens in GB/s;
+  e2e           the same step through the Python API with host (pinned) inputs
+                and outputs, copies inside the timed region;
+  cpu_baseline  the fp64 oracle on the host cores, on a bounded sample.
+
+`--impl reference` times the oracle alone (the reference arm).
+Under torchrun, every rank runs its own replica of the workload (its own
+sequences; weak scaling) and the time is the maximum over ranks.
+"""
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = ("paged decode attn HBM GB/s (% of peak) & seq·layer/s; "
+          "prefill attn TFLOP/s")
+LAYERS = W.NUM_LAYERS
+DECODE_SEQS = 64
+DECODE_CTX = 640
+
+
+# ---------------------------------------------------------------- arithmetic
+
+def decode_algorithmic_bytes(num_seqs, ctx, H_q=W.H_Q, H_kv=W.H_KV, D=W.HEAD_DIM, bs=256):
+    """Bytes a decode call must move at least: K and V rows of the attended
+    tokens, q, out, lse, the used block-table entries and the context length."""
+    kv = ctx * H_kv * D * 2 * 2
+    q_out = 2 * H_q * D * 2
+    lse = H_q * 4
+    table = -(-ctx // bs) * 4
+    return num_seqs * (kv + q_out + lse + table + 4)
+
+
+def kv_store_algorithmic_bytes(num_tokens, H_kv=W.H_KV, D=W.HEAD_DIM):
+    """Read k and v rows, write them into the cache, read the slot."""
+    return num_tokens * (H_kv * D * 2 * 2 * 2 + 4)
+
+
+def prefill_flops(q_lens, k_lens, H_q=W.H_Q, D=W.HEAD_DIM):
+    """4*D FLOPs per unmasked (query, key, head): Q K^T and P V."""
+    pairs = 0
+    for lq, lk in zip(q_lens, k_lens):
+        lq, lk = int(lq), int(lk)
+        pairs += lq * (lk - lq) + lq * (lq + 1) // 2
+    return 4 * D * pairs * H_q
+
+
+def weight_streaming_roof(bandwidth_bytes_s, weight_bytes, concurrency):
+    """Crude decode roof of a model that streams its weights once per step:
+    tokens/s = bandwidth / weight bytes x concurrency."""
+    return bandwidth_bytes_s / weight_bytes * concurrency
+
+
+# ---------------------------------------------------------------- environment
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                source="fallback")
+
+
+def source_digest(*names):
+    h = hashlib.sha1()
+    for n in names:
+        with open(os.path.join(ROOT, "paged_kv_attention_22_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(kernel, digest):
+    """DRAM bytes per launch from the committed ncu summary of `kernel`, if it
+    was taken from the current source (same digest); else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("source_digest") != digest:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        self.result = None
+        if self.proc is None:
+            return False
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if sm:
+            self.result = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                           "reasons": sorted(reasons), "samples": len(sm)}
+        return False
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(backend):
+    rank, world, local = dist_env()
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, device=None) -> float:
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- GPU legs
+
+def _dev(a):
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+class Sweep:
+    """The 28 layers' device state and pre-marshalled C-ABI calls."""
+
+    def __init__(self, pkv, seed_base):
+        self.pkv = pkv
+        self.L = pkv.lib()
+        self.layers = []
+        self.host_cases = []
+        for layer in range(LAYERS):
+            case = W.sweep64_layer(layer, base_seed=seed_base)
+            kc, vc = _dev(case.poisoned_pool()), _dev(case.poisoned_pool())
+            pkv.kv_store(_dev(case.history.k), _dev(case.history.v), kc, vc,
+                         _dev(case.history.slots))
+            st = case.step
+            S, H_q, D = st.q.shape
+            d = dict(kc=kc, vc=vc, q=_dev(st.q), k=_dev(st.new.k), v=_dev(st.new.v),
+                     slots=_dev(st.new.slots), bt=_dev(case.block_tables),
+                     ctx=_dev(st.context_lens), out=torch.empty((S, H_q, D), dtype=torch.bfloat16,
+                                                                 device="cuda"),
+                     lse=torch.empty((S, H_q), dtype=torch.float32, device="cuda"))
+            d["ws"] = torch.empty(pkv.decode_workspace_size(S, H_q, D, st.max_context_len),
+                                  dtype=torch.uint8, device="cuda")
+            self.layers.append(d)
+            self.host_cases.append(case)
+        torch.cuda.synchronize()
+        if pkv.check_device_errors() != 0:
+            raise RuntimeError("device error while filling the caches")
+        c0 = self.host_cases[0]
+        self.S, self.H_q, self.D = c0.step.q.shape
+        self.H_kv, self.bs, self.NB = c0.H_kv, c0.block_size, c0.num_blocks
+        self.max_ctx = c0.step.max_context_len
+        self.num_splits = pkv.decode_num_splits(self.S, self.H_q, self.H_kv, self.D, self.max_ctx)
+        self.scale = c0.scale
+
+    def calls(self, stream_handle):
+        """Per layer: (store_fn, decode_fn) closures over ctypes arguments."""
+        P = ctypes.c_void_p
+        L = self.L
+        out = []
+        for d in self.layers:
+            sargs = (P(d["k"].data_ptr()), P(d["v"].data_ptr()), P(d["kc"].data_ptr()),
+                     P(d["vc"].data_ptr()), P(d["slots"].data_ptr()), d["k"].shape[0], self.H_kv,
+                     self.D, self.bs, self.NB, P(stream_handle))
+            dargs = (P(d["q"].data_ptr()), P(d["kc"].data_ptr()), P(d["vc"].data_ptr()),
+                     P(d["bt"].data_ptr()), d["bt"].shape[1], P(d["ctx"].data_ptr()),
+                     self.max_ctx, self.S, self.H_q, self.H_kv, self.D, self.bs, self.NB,
+                     ctypes.c_float(self.scale), P(d["out"].data_ptr()), P(d["lse"].data_ptr()),
+                     P(d["ws"].data_ptr()), d["ws"].numel(), P(stream_handle))
+            out.append((sargs, dargs))
+        return out
+
+    def run_step(self, calls, events=None):
+        L = self.L
+        for i, (sargs, dargs) in enumerate(calls):
+            if L.pkv_kv_store(*sargs) != 0:
+                raise RuntimeError("pkv_kv_store failed")
+            if events is not None:
+                events[i][0].record()
+            if L.pkv_paged_decode_attn(*dargs) != 0:
+                raise RuntimeError("pkv_paged_decode_attn failed: " +
+                                   L.pkv_last_cuda_error().decode())
+            if events is not None:
+                events[i][1].record()
+
+
+def time_sweep(sweep, steps, warmup, device):
+    stream = torch.cuda.current_stream()
+    calls = sweep.calls(stream.cuda_stream)
+    for _ in range(warmup):
+        sweep.run_step(calls)
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(LAYERS)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for k in range(steps):
+        sweep.run_step(calls, ev[k])
+    end.record()
+    torch.cuda.synchronize()
+    barrier()
+    total_ms = start.elapsed_time(end)
+    decode_ms = [a.elapsed_time(b) for row in ev for a, b in row]
+    return total_ms, decode_ms
+
+
+def time_sweep_graph(sweep, steps, warmup):
+    """The same step captured once into a CUDA graph and replayed."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        calls = sweep.calls(s.cuda_stream)
+        sweep.run_step(calls)  # warm the stream before capture
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
+            sweep.run_step(sweep.calls(s.cuda_stream))
+    torch.cuda.synchronize()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        g.replay()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def time_e2e(sweep, steps, warmup):
+    """Through the Python API with pinned host inputs/outputs: per step, copy
+    every layer's q, new k, new v and slots in, run, copy out and lse back."""
+    pkv = sweep.pkv
+    hosts = []
+    for d in sweep.layers:
+        hosts.append({k: d[k].cpu().pin_memory() for k in ("q", "k", "v", "slots")})
+    outs = [(torch.empty_like(d["out"], device="cpu").pin_memory(),
+             torch.empty_like(d["lse"], device="cpu").pin_memory()) for d in sweep.layers]
+    staging = [{k: torch.empty_like(d[k]) for k in ("q", "k", "v", "slots")} for d in sweep.layers]
+    h2d = sum(t.numel() * t.element_size() for h in hosts for t in h.values())
+    d2h = sum(o.numel() * o.element_size() + l.numel() * l.element_size() for o, l in outs)
+
+    def step():
+        for d, h, stg, (ho, hl) in zip(sweep.layers, hosts, staging, outs):
+            for k in ("q", "k", "v", "slots"):
+                stg[k].copy_(h[k], non_blocking=True)
+            pkv.kv_store(stg["k"], stg["v"], d["kc"], d["vc"], stg["slots"])
+            pkv.paged_decode_attn(stg["q"], d["kc"], d["vc"], d["bt"], d["ctx"], sweep.max_ctx,
+                                  sweep.scale, out=d["out"], lse=d["lse"], workspace=d["ws"])
+            ho.copy_(d["out"], non_blocking=True)
+            hl.copy_(d["lse"], non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end), h2d, d2h
+
+
+def time_prefill(pkv, steps, warmup):
+    """Prefix-cached prefill: store of the 32768 prompt tokens, then prefill."""
+    pre, _ = W.prefix8k()
+    kc, vc = _dev(pre.poisoned_pool()), _dev(pre.poisoned_pool())
+    pkv.kv_store(_dev(pre.history.k), _dev(pre.history.v), kc, vc, _dev(pre.history.slots))
+    st = pre.step
+    k, v, slots = _dev(st.new.k), _dev(st.new.v), _dev(st.new.slots)
+    q, cq, ck, bt = _dev(st.q), _dev(st.cu_seqlens_q), _dev(st.cu_seqlens_k), _dev(pre.block_tables)
+    out = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], q.shape[1]), dtype=torch.float32, device="cuda")
+    n = max(steps, 5)
+    store_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(n)]
+    pre_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+
+    def once(i=None):
+        if i is not None:
+            store_ev[i][0].record()
+        pkv.kv_store(k, v, kc, vc, slots)
+        if i is not None:
+            store_ev[i][1].record()
+            pre_ev[i][0].record()
+        pkv.paged_prefill_attn(q, kc, vc, cq, ck, bt, st.max_seqlen_q, st.max_seqlen_k, pre.scale,
+                               out=out, lse=lse)
+        if i is not None:
+            pre_ev[i][1].record()
+
+    for _ in range(max(warmup, 3)):
+        once()
+    torch.cuda.synchronize()
+    for i in range(n):
+        once(i)
+    torch.cuda.synchronize()
+    if pkv.check_device_errors() != 0:
+        raise RuntimeError("device error in the prefill leg")
+    store_ms = statistics.median(a.elapsed_time(b) for a, b in store_ev)
+    pre_ms = statistics.median(a.elapsed_time(b) for a, b in pre_ev)
+    flops = prefill_flops(np.diff(st.cu_seqlens_q), np.diff(st.cu_seqlens_k))
+    store_bytes = kv_store_algorithmic_bytes(st.new.num_tokens)
+    return dict(prefill_ms=pre_ms, flops=flops, store_ms=store_ms, store_bytes=store_bytes,
+                launches=2 * n)
+
+
+# ---------------------------------------------------------------- CPU (oracle) legs
+
+def oracle_sample(seconds_target=12.0, layers=4, seed_base=4000):
+    """The fp64 oracle on a bounded sample of the sweep: `layers` layers of the
+    64-sequence decode step (store + attention), repeated until about
+    seconds_target seconds of host work. Returns (seq*layer/s, threads, desc)."""
+    import oracle
+    cases = [W.sweep64_layer(l, base_seed=seed_base) for l in range(layers)]
+    caches = []
+    for c in cases:
+        kc, vc = c.poisoned_pool(), c.poisoned_pool()
+        oracle.kv_store(c.history.k, c.history.v, kc, vc, c.history.slots)
+        caches.append((kc, vc))
+    done, t0 = 0, time.perf_counter()
+    while True:
+        for c, (kc, vc) in zip(cases, caches):
+            st = c.step
+            oracle.kv_store(st.new.k, st.new.v, kc, vc, st.new.slots)
+            oracle.decode(st.q, kc, vc, c.block_tables, st.context_lens, c.scale)
+            done += 1
+        el = time.perf_counter() - t0
+        if el >= seconds_target:
+            break
+    seq_layers = done * DECODE_SEQS
+    desc = (f"{done} layer-steps ({layers} distinct layers) of the c=64 ctx-640 decode sweep, "
+            f"{seq_layers} seq*layer in {el:.1f} s")
+    return seq_layers / el, oracle.num_threads(), desc
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    per_step = []
+    cases = [W.sweep64_layer(0)]
+    kc, vc = cases[0].poisoned_pool(), cases[0].poisoned_pool()
+    c = cases[0]
+    oracle.kv_store(c.history.k, c.history.v, kc, vc, c.history.slots)
+    st = c.step
+
+    def step():
+        oracle.kv_store(st.new.k, st.new.v, kc, vc, st.new.slots)
+        oracle.decode(st.q, kc, vc, c.block_tables, st.context_lens, c.scale)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        t1 = time.perf_counter()
+        step()
+        per_step.append(time.perf_counter() - t1)
+    total = time.perf_counter() - t0
+    value = args.steps * DECODE_SEQS / total
+    sample = ("each step: layer 0 of the 28-layer c=64 ctx-640 decode sweep "
+              "(KV store of 64 tokens + decode of 64 sequences), fp64 oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "seq·layer/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode sweep c=64 ctx=640, 28 layers, bs=256, 16q/8kv x 128",
+                   "sample": "one layer per step"},
+        "cpu_baseline": {"value": value, "unit": "seq·layer/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "seq·layer/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import paged_kv_attention_22_gb300 as pkv
+    from paged_kv_attention_22_gb300 import build as pkv_build
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dist_init("nccl")
+    if rank == 0:
+        pkv_build.build()
+    barrier()
+    pkv.lib()
+
+    # CPU baseline before any heavy GPU work (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, desc = oracle_sample()
+        cpu = {"value": v, "unit": "seq·layer/s", "cores": cores, "kind": "oracle",
+               "sample": desc}
+
+    peaks = load_peaks()
+    sweep = Sweep(pkv, seed_base=4000 + 1000 * rank)
+    with ClockSampler(local) as clocks:
+        total_ms, decode_ms = time_sweep(sweep, args.steps, args.warmup, local)
+    graph_ms = time_sweep_graph(sweep, args.steps, args.warmup)
+    if pkv.check_device_errors() != 0:
+        raise RuntimeError("device error during the timed region")
+
+    t_max = max_over_ranks(total_ms / 1000.0, device="cuda")
+    g_max = max_over_ranks(graph_ms / 1000.0, device="cuda")
+    units = sum_over_ranks(args.steps * LAYERS * DECODE_SEQS, device="cuda")
+    value_eager = units / t_max
+    value_graph = units / g_max
+
+    dec_bytes = decode_algorithmic_bytes(DECODE_SEQS, DECODE_CTX)
+    dec_s = statistics.mean(decode_ms) / 1000.0
+    achieved = dec_bytes / dec_s / 1e9
+    digest = source_digest("decode.cu", "ptx.cuh")
+    traffic = profiled_traffic("decode_split", digest)
+
+    e2e = None
+    if not args.no_e2e:
+        e_ms, h2d, d2h = time_e2e(sweep, max(args.steps // 4, 10), args.warmup)
+        n_e2e = max(args.steps // 4, 10)
+        e_max = max_over_ranks(e_ms / 1000.0, device="cuda")
+        e_units = sum_over_ranks(n_e2e * LAYERS * DECODE_SEQS, device="cuda")
+        e2e = {"value": e_units / e_max, "unit": "seq·layer/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "path": "python API, pinned host buffers"}
+
+    prefill = None
+    if not args.no_prefill:
+        pr = time_prefill(pkv, min(args.steps, 20), args.warmup)
+        tflops = pr["flops"] / (pr["prefill_ms"] / 1000.0) / 1e12
+        store_gbs = pr["store_bytes"] / (pr["store_ms"] / 1000.0) / 1e9
+        prefill = {"workload": "prefix-cached prefill: 8 seqs x 4096 new tokens over a shared "
+                               "4096-token cached prefix (Lk 8192), bs=256",
+                   "value": tflops, "unit": "TFLOP/s", "ms_per_call": pr["prefill_ms"],
+                   "flops_per_call": pr["flops"],
+                   "frac": tflops / peaks["bf16_tflops"], "peak": peaks["bf16_tflops"],
+                   "peak_kind": f"bf16 dense burst ({peaks['source']})",
+                   "kv_store_gbs": store_gbs,
+                   "kv_store_frac": store_gbs / peaks["hbm_gbs"],
+                   "kv_store_tokens": 32768}
+
+    launches_per_step = LAYERS * (2 + (1 if sweep.num_splits > 1 else 0))
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": value_graph,
+            "unit": "seq·layer/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": 1000.0 * g_max / args.steps,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "decode sweep c=64: 64 seqs x ctx 640, 28 distinct layer "
+                                   "caches, bs=256, 16 q / 8 kv heads x 128, KV store + decode "
+                                   "per layer",
+                       "timing": "CUDA graph of one step, replayed",
+                       "l2": "inputs larger than L2 (4.7 GB of K/V per step)",
+                       "decode_splits": sweep.num_splits},
+            "eager": {"value": value_eager, "ms_per_step": 1000.0 * t_max / args.steps},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": traffic,
+                         "kernel": "decode call (split + merge)",
+                         "algorithmic_bytes_per_launch": dec_bytes,
+                         "us_per_launch": dec_s * 1e6,
+                         "peak_kind": f"HBM copy ({peaks['source']})"},
+            "prefill": prefill,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.result,
+        }
+        print(json.dumps(line))
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,199 @@
+/*
+ * pkv.h -- paged-KV-cache attention for GB300 (sm_103a): the C ABI of libpkv.so.
+ *
+ * The pages describe a nano-vLLM style serving engine whose scheduler asks a
+ * KV block manager for cache blocks ("How lunaryes/nano-vllm works",
+ * Connections: "Scheduler -> KV Block Manager: allocates cached blocks") and
+ * whose model runner sets an execution context before running the Qwen3
+ * layers (same page, Connections: "Model Runner -> Execution Context"). This
+ * library is the data-parallel hot path inside those layers: writing each
+ * step's new K/V rows into the paged cache (the "paged KV cache" of the
+ * nano-vllm-rs README, "GGUF Models"), q=1 decode attention (the q=1 decode
+ * kernel of the nano-vllm-sansho README, "Sansho Serving Roofline Anchors") and
+ * varlen causal prefill attention that also serves prompts whose leading blocks
+ * are already cached (prefix caching: nano-vllm-sansho README, "Key Features").
+ * Its arguments are that execution context: slot mapping, block tables,
+ * context lengths, cumulative sequence lengths.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Layout. bf16 everywhere for tensors; row-major, contiguous.
+ *   new K/V rows   k, v        [T, H_kv, D]
+ *   cache          k_cache     [num_blocks, block_size, H_kv, D]  (same for v_cache)
+ *   queries        q           [T_q, H_q, D] (prefill) or [S, H_q, D] (decode)
+ *   outputs        out         like q; lse float32 [rows, H_q]
+ *   block tables   int32       [S, max_blocks_per_seq]; entry -1 = no block
+ * Slot of token at position p of sequence s:
+ *   block_tables[s][p / block_size] * block_size + p % block_size.
+ * Query head h reads KV head h / (H_q / H_kv).
+ * D must be 128, block_size a multiple of 16, H_q / H_kv in {1, 2, 4}.
+ *
+ * Memory and ownership. Every pointer is caller-owned device memory (except
+ * the host pointer flags_out); the library allocates and frees nothing, keeps
+ * no per-call state, and returns before the kernels finish. Device buffers
+ * must be 16-byte aligned.
+ *
+ * Streams. `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ * default stream). Every call only enqueues work on that stream and never
+ * synchronises, so it may be captured into a CUDA graph, except
+ * pkv_check_device_errors, which synchronises the stream.
+ *
+ * Errors. Arguments the host can see are checked before anything is enqueued:
+ * PKV_ERR_INVALID_ARG (null pointer, negative size, inconsistent shape),
+ * PKV_ERR_UNSUPPORTED (a shape this build has no kernel for),
+ * PKV_ERR_WORKSPACE_TOO_SMALL. A failing CUDA call gives PKV_ERR_CUDA and
+ * pkv_last_cuda_error() names it (thread-local). Values that live on the device
+ * (slots, table entries, lengths) are checked by the kernels: an invalid one
+ * skips the access it would have made and raises a bit of the device error
+ * word (PKV_DEVERR_*), read with pkv_check_device_errors. Outputs that depend
+ * on an invalid value are undefined; nothing outside the given buffers is
+ * touched.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,
+  PKV_ERR_UNSUPPORTED = 2,
+  PKV_ERR_WORKSPACE_TOO_SMALL = 3,
+  PKV_ERR_CUDA = 4
+} pkv_status;
+
+/* Bits of the device error word. */
+#define PKV_DEVERR_SLOT 0x1u      /* a slot outside [-1, num_blocks * block_size)      */
+#define PKV_DEVERR_BLOCK 0x2u     /* a needed block-table entry outside [0, num_blocks) */
+#define PKV_DEVERR_CONTEXT 0x4u   /* context_len <= 0, above max_context_len or above
+                                     max_blocks_per_seq * block_size                  */
+#define PKV_DEVERR_SEQLENS 0x8u   /* cu_seqlens inconsistent with the host-side maxima  */
+#define PKV_DEVERR_TIMEOUT 0x10u  /* a kernel gave up waiting on one of its barriers    */
+
+/* Name of a status code (static string). */
+const char *pkv_status_string(pkv_status status);
+
+/* The CUDA error string of this thread's last PKV_ERR_CUDA, or "" if none. */
+const char *pkv_last_cuda_error(void);
+
+/*
+ * KV store: the slot-mapping scatter of the new tokens' K/V rows into the
+ * cache. k_cache[slot_mapping[t]] = k[t] and v_cache[slot_mapping[t]] = v[t]
+ * for every t with slot_mapping[t] >= 0 (all H_kv * D values of the row, bit
+ * for bit); -1 skips the token (the block manager gave it no slot, as for
+ * tokens of a cached prefix). Two tokens with the same non-negative slot in one
+ * call race. A slot below -1 or at/above num_blocks * block_size is skipped
+ * and raises PKV_DEVERR_SLOT.
+ *   k, v           device bf16 [num_tokens, num_kv_heads, head_dim]
+ *   k_cache,v_cache device bf16 [num_blocks, block_size, num_kv_heads, head_dim]
+ *   slot_mapping   device int32 [num_tokens]
+ * num_tokens == 0 is a no-op. Here head_dim may be any value with
+ * num_kv_heads * head_dim * 2 a multiple of 16 bytes.
+ */
+pkv_status pkv_kv_store(const void *k, const void *v, void *k_cache, void *v_cache,
+                        const int32_t *slot_mapping, int32_t num_tokens,
+                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                        int64_t num_blocks, void *stream);
+
+/*
+ * Bytes of device workspace that pkv_paged_decode_attn needs for these sizes
+ * (0 on invalid sizes). The workspace holds the per-split partial results of
+ * the split-K kernel; the caller allocates it once and may reuse it for every
+ * call with sizes no larger than these.
+ */
+size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t max_context_len);
+
+/*
+ * Paged decode attention, one query token per sequence (q=1 decode).
+ * For sequence s, query head h and KV head g = h / (H_q / H_kv):
+ *   z_p   = scale * <q[s,h], k_cache[slot(s, p), g]>   for p < context_lens[s]
+ *   out   = sum_p exp(z_p - M) v_cache[slot(s,p), g] / sum_p exp(z_p - M)
+ *   lse   = M + ln sum_p exp(z_p - M),   M = max_p z_p      (natural log)
+ * The query's own K/V must already be in the cache (store first, then attend,
+ * on the same stream). Split-K over the context ("flash decoding"): partial
+ * results go to the workspace and a second kernel merges them.
+ *   q              device bf16 [num_seqs, num_q_heads, head_dim]
+ *   block_tables   device int32 [num_seqs, max_blocks_per_seq]
+ *   context_lens   device int32 [num_seqs], each in [1, max_context_len]
+ *   max_context_len host int: an upper bound of context_lens (sizes the grid)
+ *   scale          the logit scale (usually 1/sqrt(head_dim))
+ *   out            device bf16 [num_seqs, num_q_heads, head_dim]
+ *   lse            device float32 [num_seqs, num_q_heads], or NULL
+ *   workspace      device, >= pkv_decode_workspace_size(...) bytes, 16-byte aligned
+ * Rows whose context_len is invalid raise PKV_DEVERR_CONTEXT and are not written.
+ */
+pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *context_lens, int32_t max_context_len,
+                                 int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                 float scale, void *out, float *lse, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/*
+ * Number of splits (partial results per query row) that pkv_paged_decode_attn
+ * uses for these sizes on the current device; 1 means the merge kernel is not
+ * launched. Returns -1 on invalid sizes or a CUDA error.
+ */
+int32_t pkv_decode_num_splits(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t max_context_len);
+
+/*
+ * Tuning knob of the decode kernel: the number of 32-key chunks per split
+ * (0 = automatic, the default). Process-wide; not thread-safe against
+ * concurrent launches. Values are clamped to [2, 1024].
+ */
+void pkv_decode_set_chunks_per_split(int32_t chunks);
+
+/*
+ * Bytes of device workspace that pkv_paged_prefill_attn needs (currently 0 for
+ * every size: the prefill kernel keeps all its state on chip).
+ */
+size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t max_seqlen_q);
+
+/*
+ * Varlen causal prefill attention over the paged cache, with prefix caching.
+ * Segment s has Lq = cu_seqlens_q[s+1] - cu_seqlens_q[s] query tokens
+ * (rows cu_seqlens_q[s] .. of q) and Lk = cu_seqlens_k[s+1] - cu_seqlens_k[s]
+ * keys, read through block_tables[s]; the queries are the last Lq of the Lk
+ * positions, so query i sees keys p <= Lk - Lq + i (bottom-right causal;
+ * Lq == Lk is plain causal attention, Lq < Lk serves a prompt whose first
+ * Lk - Lq tokens are cached). Keys are always read from the cache: store the
+ * prompt's new K/V first, on the same stream. Lq == 0 writes nothing.
+ * Output and lse as in decode, for every query row.
+ *   q              device bf16 [total_q, num_q_heads, head_dim]
+ *   cu_seqlens_q/k device int32 [num_seqs + 1], non-decreasing, from 0
+ *   max_seqlen_q/k host ints: upper bounds of Lq and Lk (size the grid)
+ *   out            device bf16 [total_q, num_q_heads, head_dim]
+ *   lse            device float32 [total_q, num_q_heads], or NULL
+ *   workspace      may be NULL when pkv_prefill_workspace_size returns 0
+ * Segments with Lq > Lk, Lq > max_seqlen_q, Lk > max_seqlen_k or Lk beyond
+ * the table raise PKV_DEVERR_SEQLENS and are not written.
+ */
+pkv_status pkv_paged_prefill_attn(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                  const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
+                                  int32_t max_seqlen_k, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int64_t num_blocks, float scale, void *out, float *lse,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronise `stream`, then return in *flags_out the OR of the device error
+ * words of every kernel of this library on the current device, and clear
+ * them. For tests and debugging: it blocks the host.
+ */
+pkv_status pkv_check_device_errors(void *stream, uint32_t *flags_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

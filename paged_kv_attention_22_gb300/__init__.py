@@ -1,0 +1,223 @@
+"""Paged-KV-cache attention for GB300 (sm_103a): Python binding of libpkv.so.
+
+The functions here have the names of the C entry points in ``include/pkv.h``
+and do argument marshalling only: they check dtypes and shapes of torch
+tensors, pass their device pointers and the current CUDA stream to the C ABI,
+and allocate outputs the caller did not supply. Every step of the computation
+runs in the library's CUDA kernels. There is no fallback: if libpkv.so has not
+been built, or a call fails, an exception is raised.
+
+Tensors (all CUDA, contiguous):
+    k, v           bf16 [T, H_kv, 128]       new K/V rows
+    k_cache,v_cache bf16 [num_blocks, block_size, H_kv, 128]
+    slot_mapping   int32 [T]
+    q              bf16 [S, H_q, 128] (decode) or [T_q, H_q, 128] (prefill)
+    block_tables   int32 [S, max_blocks_per_seq], -1 padded
+    context_lens   int32 [S]
+    cu_seqlens_q/k int32 [S + 1]
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_OK = 0
+PKV_ERR_INVALID_ARG = 1
+PKV_ERR_UNSUPPORTED = 2
+PKV_ERR_WORKSPACE_TOO_SMALL = 3
+PKV_ERR_CUDA = 4
+
+DEVERR_SLOT = 0x1
+DEVERR_BLOCK = 0x2
+DEVERR_CONTEXT = 0x4
+DEVERR_SEQLENS = 0x8
+DEVERR_TIMEOUT = 0x10
+
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        name = status_string(status)
+        detail = lib().pkv_last_cuda_error().decode() if status == PKV_ERR_CUDA else ""
+        super().__init__(f"{what}: {name}" + (f" ({detail})" if detail else ""))
+
+
+def lib():
+    """The loaded libpkv.so (ctypes), with argument types declared."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIBRARY_PATH):
+        raise ImportError(
+            f"{LIBRARY_PATH} is missing: build it with "
+            "`python -m paged_kv_attention_22_gb300.build` (nvcc, sm_103a)")
+    L = ctypes.CDLL(LIBRARY_PATH)
+    P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+    L.pkv_status_string.argtypes = [ctypes.c_int]
+    L.pkv_status_string.restype = ctypes.c_char_p
+    L.pkv_last_cuda_error.argtypes = []
+    L.pkv_last_cuda_error.restype = ctypes.c_char_p
+    L.pkv_kv_store.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i64, P]
+    L.pkv_kv_store.restype = ctypes.c_int
+    L.pkv_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+    L.pkv_decode_workspace_size.restype = sz
+    L.pkv_paged_decode_attn.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64,
+                                        f32, P, P, P, sz, P]
+    L.pkv_paged_decode_attn.restype = ctypes.c_int
+    L.pkv_decode_num_splits.argtypes = [i32, i32, i32, i32, i32]
+    L.pkv_decode_num_splits.restype = i32
+    L.pkv_decode_set_chunks_per_split.argtypes = [i32]
+    L.pkv_decode_set_chunks_per_split.restype = None
+    L.pkv_prefill_workspace_size.argtypes = [i32, i32]
+    L.pkv_prefill_workspace_size.restype = sz
+    L.pkv_paged_prefill_attn.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                         i32, i32, i64, f32, P, P, P, sz, P]
+    L.pkv_paged_prefill_attn.restype = ctypes.c_int
+    L.pkv_check_device_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    L.pkv_check_device_errors.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().pkv_status_string(int(status)).decode()
+
+
+def _check(status, what):
+    if status != PKV_OK:
+        raise PkvError(status, what)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _need(t, name, dtype, ndim):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def kv_store(k, v, k_cache, v_cache, slot_mapping, stream=None):
+    """Scatter k, v [T, H_kv, D] into the caches at slot_mapping (-1: skip)."""
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    NB, bs, H_kv, D = k_cache.shape
+    if v_cache.shape != k_cache.shape or k.shape != v.shape or k.shape[1:] != (H_kv, D) \
+            or slot_mapping.shape[0] != k.shape[0]:
+        raise ValueError("inconsistent shapes")
+    _check(lib().pkv_kv_store(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
+                              k.shape[0], H_kv, D, bs, NB, _stream(stream)), "pkv_kv_store")
+
+
+def decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len) -> int:
+    return int(lib().pkv_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len))
+
+
+def decode_num_splits(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len) -> int:
+    """Splits the decode call would use on the current device (1: no merge kernel)."""
+    n = int(lib().pkv_decode_num_splits(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                        max_context_len))
+    if n < 0:
+        raise PkvError(PKV_ERR_CUDA, "pkv_decode_num_splits")
+    return n
+
+
+def decode_set_chunks_per_split(chunks: int) -> None:
+    """Tuning knob: 32-key chunks per decode split (0 = automatic)."""
+    lib().pkv_decode_set_chunks_per_split(int(chunks))
+
+
+def paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
+                      out=None, lse=None, workspace=None, stream=None, with_lse=True):
+    """q=1 decode attention through block tables. Returns (out, lse)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    S, H_q, D = q.shape
+    NB, bs, H_kv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is None and with_lse:
+        lse = torch.empty((S, H_q), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    need = decode_workspace_size(S, H_q, D, int(max_context_len))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8, 1)
+    _check(lib().pkv_paged_decode_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), int(max_context_len), S, H_q, H_kv, D, bs, NB, float(scale),
+        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)),
+        "pkv_paged_decode_attn")
+    return out, lse
+
+
+def prefill_workspace_size(num_seqs, max_seqlen_q) -> int:
+    return int(lib().pkv_prefill_workspace_size(num_seqs, max_seqlen_q))
+
+
+def paged_prefill_attn(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables,
+                       max_seqlen_q, max_seqlen_k, scale, out=None, lse=None, workspace=None,
+                       stream=None, with_lse=True):
+    """Varlen causal prefill over the paged cache (bottom-right aligned). Returns (out, lse)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    T, H_q, D = q.shape
+    NB, bs, H_kv, _ = k_cache.shape
+    S = cu_seqlens_q.shape[0] - 1
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is None and with_lse:
+        lse = torch.empty((T, H_q), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    need = prefill_workspace_size(S, int(max_seqlen_q))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(lib().pkv_paged_prefill_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        _ptr(block_tables), block_tables.shape[1], S, T, int(max_seqlen_q), int(max_seqlen_k),
+        H_q, H_kv, D, bs, NB, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() if workspace is not None else 0, _stream(stream)),
+        "pkv_paged_prefill_attn")
+    return out, lse
+
+
+def check_device_errors(stream=None) -> int:
+    """Synchronise, then return and clear the OR of the kernels' device error words."""
+    flags = ctypes.c_uint32(0)
+    _check(lib().pkv_check_device_errors(_stream(stream), ctypes.byref(flags)),
+           "pkv_check_device_errors")
+    return int(flags.value)

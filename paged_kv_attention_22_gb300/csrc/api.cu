@@ -1,0 +1,357 @@
+// The C ABI of libpkv.so (declared in include/pkv.h): argument checks, launch
+// planning, TMA descriptor encoding and error reporting around the kernels.
+// Allocates nothing; every call only enqueues work on the caller's stream.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/pkv.h"
+#include "internal.h"
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+pkv_status cuda_fail(cudaError_t e, const char *where) {
+  snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s (%s)", where,
+           cudaGetErrorName(e), cudaGetErrorString(e));
+  return PKV_ERR_CUDA;
+}
+
+pkv_status cu_fail(CUresult r, const char *where) {
+  snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: CUresult %d", where,
+           static_cast<int>(r));
+  return PKV_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- device facts
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+pkv_status current_sm_count(int *sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice, "device index");
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    int major = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major < 10) {
+      snprintf(g_last_cuda_error, sizeof g_last_cuda_error,
+               "device %d has compute capability %d.x; this library is built for sm_103a", dev,
+               major);
+      return PKV_ERR_CUDA;
+    }
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
+  }
+  *sms = n;
+  return PKV_OK;
+}
+
+// ---------------------------------------------------------------- TMA descriptors
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+pkv_status get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn) {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                    cudaEnableDefault, &q);
+    if (g_encode_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
+      g_encode_err = cudaErrorNotSupported;
+    if (g_encode_err == cudaSuccess) g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  if (g_encode == nullptr) return cuda_fail(g_encode_err, "cuTensorMapEncodeTiled entry point");
+  *fn = g_encode;
+  return PKV_OK;
+}
+
+// A 3-D bf16 view [rows, heads, dim] (dim innermost, contiguous) with a box of
+// box_dim x 1 head x box_rows rows.
+pkv_status encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int32_t heads,
+                           int32_t dim, uint32_t box_dim, uint32_t box_rows, bool swizzle128) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  pkv_status st = get_encoder(&enc);
+  if (st != PKV_OK) return st;
+  cuuint64_t gdim[3] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[2] = {static_cast<cuuint64_t>(dim) * 2,
+                           static_cast<cuuint64_t>(dim) * 2 * static_cast<cuuint64_t>(heads)};
+  cuuint32_t box[3] = {box_dim, 1, box_rows};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), gdim,
+                   gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cu_fail(r, "cuTensorMapEncodeTiled");
+  return PKV_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+std::atomic<int32_t> g_decode_chunks_override{0};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Sizes shared by the attention calls.
+pkv_status check_attention_shape(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t block_size, int64_t num_blocks, int32_t max_blocks) {
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      num_blocks <= 0 || max_blocks <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_UNSUPPORTED;
+  const int32_t G = num_q_heads / num_kv_heads;
+  if (G != 1 && G != 2 && G != 4) return PKV_ERR_UNSUPPORTED;
+  if (head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (block_size % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (num_q_heads > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  // cache rows are addressed with 32-bit TMA coordinates
+  if (num_blocks * static_cast<int64_t>(block_size) > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_blocks) * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Decode workspace layout: lse partials first, then output partials, both
+// sized for the largest split count any plan can choose.
+struct DecodeWorkspace {
+  size_t lse_bytes, o_offset, total;
+};
+
+bool decode_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                             int32_t max_context_len, DecodeWorkspace *w) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len <= 0) return false;
+  const int64_t min_keys = static_cast<int64_t>(pkv::kDecodeChunk) * pkv::kDecodeMinChunksPerSplit;
+  const int64_t j_max = (max_context_len + min_keys - 1) / min_keys;
+  const int64_t rows = static_cast<int64_t>(num_seqs) * num_q_heads;
+  w->lse_bytes = static_cast<size_t>(rows * j_max) * sizeof(float);
+  w->o_offset = align_up(w->lse_bytes, 256);
+  w->total = w->o_offset + static_cast<size_t>(rows * j_max * head_dim) * sizeof(float);
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pkv_status_string(pkv_status status) {
+  switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    case PKV_ERR_WORKSPACE_TOO_SMALL: return "PKV_ERR_WORKSPACE_TOO_SMALL";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+  }
+  return "PKV_ERR_UNKNOWN";
+}
+
+const char *pkv_last_cuda_error(void) { return g_last_cuda_error; }
+
+pkv_status pkv_kv_store(const void *k, const void *v, void *k_cache, void *v_cache,
+                        const int32_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t block_size, int64_t num_blocks, void *stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (k_cache == nullptr || v_cache == nullptr) return PKV_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (k == nullptr || v == nullptr || slot_mapping == nullptr))
+    return PKV_ERR_INVALID_ARG;
+  const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * 2;
+  if (row_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  pkv::KvStoreArgs a;
+  a.k = k;
+  a.v = v;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.slot_mapping = slot_mapping;
+  a.num_tokens = num_tokens;
+  a.row_vec16 = static_cast<int32_t>(row_bytes / 16);
+  a.num_slots = num_blocks * block_size;
+  cudaError_t e = pkv::launch_kv_store(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_store launch");
+  return PKV_OK;
+}
+
+size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t max_context_len) {
+  DecodeWorkspace w;
+  if (!decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_context_len, &w)) return 0;
+  return w.total;
+}
+
+int32_t pkv_decode_num_splits(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t max_context_len) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      max_context_len <= 0)
+    return -1;
+  int sms = 0;
+  if (current_sm_count(&sms) != PKV_OK) return -1;
+  pkv::DecodeArgs a{};
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.max_context_len = max_context_len;
+  const int64_t kps = static_cast<int64_t>(pkv::decode_chunks_per_split(
+                          a, sms, g_decode_chunks_override.load(std::memory_order_relaxed))) *
+                      pkv::kDecodeChunk;
+  return static_cast<int32_t>((max_context_len + kps - 1) / kps);
+}
+
+void pkv_decode_set_chunks_per_split(int32_t chunks) {
+  g_decode_chunks_override.store(chunks < 0 ? 0 : chunks, std::memory_order_relaxed);
+}
+
+pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *context_lens, int32_t max_context_len,
+                                 int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                 float scale, void *out, float *lse, void *workspace,
+                                 size_t workspace_bytes, void *stream) {
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_tables == nullptr ||
+      context_lens == nullptr || out == nullptr)
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs <= 0 || max_context_len <= 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  pkv_status st = check_attention_shape(num_q_heads, num_kv_heads, head_dim, block_size,
+                                        num_blocks, max_blocks_per_seq);
+  if (st != PKV_OK) return st;
+  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PKV_ERR_INVALID_ARG;
+  DecodeWorkspace w;
+  decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_context_len, &w);
+  if (workspace == nullptr || workspace_bytes < w.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return PKV_ERR_INVALID_ARG;
+
+  int sms = 0;
+  if ((st = current_sm_count(&sms)) != PKV_OK) return st;
+  pkv::DecodeArgs a;
+  a.q = q;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = out;
+  a.lse = lse;
+  a.ws_lse = static_cast<float *>(workspace);
+  a.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.o_offset);
+  a.max_blocks = max_blocks_per_seq;
+  a.max_context_len = max_context_len;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.num_blocks = static_cast<int32_t>(num_blocks);
+  a.scale_log2 = scale * kLog2e;
+  a.chunks_per_split = pkv::decode_chunks_per_split(
+      a, sms, g_decode_chunks_override.load(std::memory_order_relaxed));
+  const int64_t kps = static_cast<int64_t>(a.chunks_per_split) * pkv::kDecodeChunk;
+  a.num_splits = static_cast<int32_t>((max_context_len + kps - 1) / kps);
+  if (a.num_splits > 65535) return PKV_ERR_UNSUPPORTED;
+
+  CUtensorMap kmap, vmap;
+  const int64_t rows = num_blocks * block_size;
+  if ((st = encode_rows_map(&kmap, k_cache, rows, num_kv_heads, head_dim, 128, 16, false)) != PKV_OK)
+    return st;
+  if ((st = encode_rows_map(&vmap, v_cache, rows, num_kv_heads, head_dim, 128, 16, false)) != PKV_OK)
+    return st;
+  cudaError_t e = pkv::launch_decode(a, kmap, vmap, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return PKV_OK;
+}
+
+size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t max_seqlen_q) {
+  (void)num_seqs;
+  (void)max_seqlen_q;
+  return 0;
+}
+
+pkv_status pkv_paged_prefill_attn(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                  const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
+                                  int32_t max_seqlen_k, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int64_t num_blocks, float scale, void *out, float *lse,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (k_cache == nullptr || v_cache == nullptr || cu_seqlens_q == nullptr ||
+      cu_seqlens_k == nullptr || block_tables == nullptr)
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || !std::isfinite(scale))
+    return PKV_ERR_INVALID_ARG;
+  if (max_seqlen_q > max_seqlen_k) return PKV_ERR_INVALID_ARG;
+  pkv_status st = check_attention_shape(num_q_heads, num_kv_heads, head_dim, block_size,
+                                        num_blocks, max_blocks_per_seq);
+  if (st != PKV_OK) return st;
+  if (total_q > 0 && (q == nullptr || out == nullptr)) return PKV_ERR_INVALID_ARG;
+  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return PKV_OK;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PKV_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = current_sm_count(&sms)) != PKV_OK) return st;
+
+  pkv::PrefillArgs a;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.cu_seqlens_k = cu_seqlens_k;
+  a.block_tables = block_tables;
+  a.out = out;
+  a.lse = lse;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.total_q = total_q;
+  a.max_seqlen_q = max_seqlen_q;
+  a.max_seqlen_k = max_seqlen_k;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.num_blocks = static_cast<int32_t>(num_blocks);
+  a.scale_log2 = scale * kLog2e;
+
+  CUtensorMap qmap, kmap, vmap;
+  const int64_t rows = num_blocks * block_size;
+  if ((st = encode_rows_map(&qmap, q, total_q, num_q_heads, head_dim, 64, 128, true)) != PKV_OK)
+    return st;
+  if ((st = encode_rows_map(&kmap, k_cache, rows, num_kv_heads, head_dim, 64, 16, true)) != PKV_OK)
+    return st;
+  if ((st = encode_rows_map(&vmap, v_cache, rows, num_kv_heads, head_dim, 64, 16, true)) != PKV_OK)
+    return st;
+  cudaError_t e = pkv::launch_prefill(a, qmap, kmap, vmap, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return PKV_OK;
+}
+
+pkv_status pkv_check_device_errors(void *stream, uint32_t *flags_out) {
+  if (flags_out == nullptr) return PKV_ERR_INVALID_ARG;
+  *flags_out = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  if ((e = pkv::take_kv_store_errors(s, flags_out)) != cudaSuccess)
+    return cuda_fail(e, "kv_store error word");
+  if ((e = pkv::take_decode_errors(s, flags_out)) != cudaSuccess)
+    return cuda_fail(e, "decode error word");
+  if ((e = pkv::take_prefill_errors(s, flags_out)) != cudaSuccess)
+    return cuda_fail(e, "prefill error word");
+  return PKV_OK;
+}
+
+}  // extern "C"

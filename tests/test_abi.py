@@ -1,0 +1,126 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/pkv.h declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import paged_kv_attention_22_gb300 as pkv
+from paged_kv_attention_22_gb300 import build as pkv_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    pkv_build.build()
+    return pkv.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for must in ("pkv_kv_store", "pkv_paged_decode_attn", "pkv_paged_prefill_attn",
+                 "pkv_decode_workspace_size", "pkv_prefill_workspace_size",
+                 "pkv_check_device_errors", "pkv_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), f"libpkv.so does not export {name}"
+
+
+def test_error_bits_match_header():
+    text = open(HEADER).read()
+    for name, val in [("SLOT", pkv.DEVERR_SLOT), ("BLOCK", pkv.DEVERR_BLOCK),
+                      ("CONTEXT", pkv.DEVERR_CONTEXT), ("SEQLENS", pkv.DEVERR_SEQLENS),
+                      ("TIMEOUT", pkv.DEVERR_TIMEOUT)]:
+        m = re.search(r"#define PKV_DEVERR_%s (0x[0-9a-fA-F]+)u" % name, text)
+        assert m and int(m.group(1), 16) == val
+
+
+def test_status_strings(L):
+    assert pkv.status_string(0) == "PKV_OK"
+    assert pkv.status_string(3) == "PKV_ERR_WORKSPACE_TOO_SMALL"
+    assert pkv.status_string(99) == "PKV_ERR_UNKNOWN"
+
+
+FAKE = ctypes.c_void_p(0x10000)  # a non-null, 16-byte aligned value never dereferenced
+
+
+def _decode(L, **kw):
+    a = dict(q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, mb=4, cl=FAKE, mcl=64, S=2, Hq=16, Hkv=8, D=128,
+             bs=16, NB=64, scale=0.088, out=FAKE, lse=None, ws=FAKE, wsb=1 << 20)
+    a.update(kw)
+    return L.pkv_paged_decode_attn(a["q"], a["kc"], a["vc"], a["bt"], a["mb"], a["cl"], a["mcl"],
+                                   a["S"], a["Hq"], a["Hkv"], a["D"], a["bs"], a["NB"],
+                                   a["scale"], a["out"], a["lse"], a["ws"], a["wsb"], None)
+
+
+def test_decode_argument_checks(L):
+    assert _decode(L, q=None) == pkv.PKV_ERR_INVALID_ARG
+    assert _decode(L, S=0) == pkv.PKV_ERR_INVALID_ARG
+    assert _decode(L, mcl=0) == pkv.PKV_ERR_INVALID_ARG
+    assert _decode(L, D=64) == pkv.PKV_ERR_UNSUPPORTED
+    assert _decode(L, Hq=12, Hkv=8) == pkv.PKV_ERR_UNSUPPORTED
+    assert _decode(L, Hq=64, Hkv=8) == pkv.PKV_ERR_UNSUPPORTED
+    assert _decode(L, bs=24) == pkv.PKV_ERR_UNSUPPORTED
+    assert _decode(L, scale=float("nan")) == pkv.PKV_ERR_INVALID_ARG
+    assert _decode(L, wsb=16) == pkv.PKV_ERR_WORKSPACE_TOO_SMALL
+    assert _decode(L, ws=None) == pkv.PKV_ERR_WORKSPACE_TOO_SMALL
+    assert _decode(L, out=ctypes.c_void_p(0x10008)) == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_decode_workspace_size_is_monotone(L):
+    a = L.pkv_decode_workspace_size(64, 16, 128, 640)
+    b = L.pkv_decode_workspace_size(64, 16, 128, 8193)
+    assert 0 < a < b
+    assert L.pkv_decode_workspace_size(0, 16, 128, 640) == 0
+    assert L.pkv_decode_workspace_size(64, 16, 128, 0) == 0
+
+
+def test_prefill_argument_checks(L):
+    def call(**kw):
+        a = dict(q=FAKE, kc=FAKE, vc=FAKE, cq=FAKE, ck=FAKE, bt=FAKE, mb=4, S=2, T=100, mq=64,
+                 mk=64, Hq=16, Hkv=8, D=128, bs=16, NB=64, scale=0.088, out=FAKE)
+        a.update(kw)
+        return L.pkv_paged_prefill_attn(a["q"], a["kc"], a["vc"], a["cq"], a["ck"], a["bt"],
+                                        a["mb"], a["S"], a["T"], a["mq"], a["mk"], a["Hq"],
+                                        a["Hkv"], a["D"], a["bs"], a["NB"], a["scale"], a["out"],
+                                        None, None, 0, None)
+    assert call(cq=None) == pkv.PKV_ERR_INVALID_ARG
+    assert call(mq=65, mk=64) == pkv.PKV_ERR_INVALID_ARG
+    assert call(D=256) == pkv.PKV_ERR_UNSUPPORTED
+    assert call(NB=1 << 28, bs=16) == pkv.PKV_ERR_UNSUPPORTED
+    # nothing to do: returns OK without touching the device
+    assert call(T=0, q=None, out=None) == pkv.PKV_OK
+    assert call(S=0) == pkv.PKV_OK
+
+
+def test_kv_store_argument_checks(L):
+    def call(**kw):
+        a = dict(k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, sm=FAKE, T=4, H=8, D=128, bs=16, NB=64)
+        a.update(kw)
+        return L.pkv_kv_store(a["k"], a["v"], a["kc"], a["vc"], a["sm"], a["T"], a["H"], a["D"],
+                              a["bs"], a["NB"], None)
+    assert call(k=None) == pkv.PKV_ERR_INVALID_ARG
+    assert call(T=-1) == pkv.PKV_ERR_INVALID_ARG
+    assert call(H=1, D=4) == pkv.PKV_ERR_UNSUPPORTED  # 8-byte rows
+    assert call(T=0, k=None, v=None, sm=None) == pkv.PKV_OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
+def test_valid_call_without_gpu_reports_cuda_error(L):
+    assert _decode(L) == pkv.PKV_ERR_CUDA
+    assert L.pkv_last_cuda_error() != b""
+    flags = ctypes.c_uint32(7)
+    assert L.pkv_check_device_errors(None, ctypes.byref(flags)) == pkv.PKV_ERR_CUDA

@@ -1,0 +1,233 @@
+"""GPU parity: the CUDA library against the fp64 oracle on the same seeded
+inputs. Cache bytes must be bit-exact over the whole (NaN-poisoned) pool;
+attention outputs within max-abs 2e-2 and mean-abs 2e-3, lse within 1e-3."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_22_gb300 as pkv
+import workloads as W
+from runners import (assert_cache_equal, assert_close, dev_bf16, dev_i32, gpu_attend, gpu_pool,
+                     gpu_run, gpu_store, host_u16, oracle_cache, oracle_run,
+                     sampled_rows_reference)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {c.name: c for c in W.all_small_cases()}
+
+
+@pytest.fixture(autouse=True)
+def _reset_knobs():
+    pkv.decode_set_chunks_per_split(0)
+    yield
+    pkv.decode_set_chunks_per_split(0)
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_cases_match_oracle(name):
+    case = SMALL[name]
+    got = gpu_run(case)
+    ref = oracle_run(case)
+    assert got["flags"] == 0
+    assert_cache_equal(got["kc"], got["vc"], ref["kc"], ref["vc"])
+    assert_close(got["out"], got["lse"], ref["out"], ref["lse"], name)
+
+
+def test_chain256_prefill_then_decode_on_one_cache():
+    pre, dec = W.chain256()
+    g1 = gpu_run(pre)
+    # decode reuses the prefill's cache: only the new token is stored
+    g2 = gpu_run(dec, g1["kc"], g1["vc"], store_history=False)
+    r1 = oracle_run(pre)
+    r2 = oracle_run(dec)
+    assert g1["flags"] == 0 and g2["flags"] == 0
+    assert_close(g1["out"], g1["lse"], r1["out"], r1["lse"], "chain prefill")
+    assert_close(g2["out"], g2["lse"], r2["out"], r2["lse"], "chain decode")
+    assert_cache_equal(g2["kc"], g2["vc"], r2["kc"], r2["vc"])
+
+
+def test_prefix8k_decode_full():
+    _, dec = W.prefix8k()
+    got = gpu_run(dec)
+    ref = oracle_run(dec)
+    assert got["flags"] == 0
+    assert_cache_equal(got["kc"], got["vc"], ref["kc"], ref["vc"])
+    assert_close(got["out"], got["lse"], ref["out"], ref["lse"], "prefix8k decode")
+
+
+def test_prefix8k_prefill_sampled_rows():
+    pre, _ = W.prefix8k()
+    got = gpu_run(pre)
+    kc, vc = oracle_cache(pre)
+    assert got["flags"] == 0
+    assert_cache_equal(got["kc"], got["vc"], kc, vc)
+    assert np.all(np.isfinite(got["out"])) and np.all(np.isfinite(got["lse"]))
+    rng = np.random.default_rng(0)
+    st = pre.step
+    rows = []
+    for s in range(pre.num_seqs):
+        a, b = int(st.cu_seqlens_q[s]), int(st.cu_seqlens_q[s + 1])
+        for r in [a, a + 1, a + 127, a + 128, b - 129, b - 1] + list(rng.integers(a, b, 6)):
+            rows.append((int(r), int(rng.integers(0, pre.H_q))))
+    ref_out, ref_lse = sampled_rows_reference(pre, kc, vc, rows)
+    idx_r = [r for r, _ in rows]
+    idx_h = [h for _, h in rows]
+    assert_close(got["out"][idx_r, idx_h], got["lse"][idx_r, idx_h], ref_out, ref_lse,
+                 "prefix8k prefill (sampled)")
+
+
+def test_sweep64_layer_full():
+    case = W.sweep64_layer(0)
+    got = gpu_run(case)
+    ref = oracle_run(case)
+    assert got["flags"] == 0
+    assert_cache_equal(got["kc"], got["vc"], ref["kc"], ref["vc"])
+    assert_close(got["out"], got["lse"], ref["out"], ref["lse"], "sweep64 layer 0")
+
+
+@pytest.mark.parametrize("chunks", [2, 3, 5, 8, 1024])
+def test_split_count_does_not_change_results(chunks):
+    case = SMALL["ragged256/decode"]
+    ref = oracle_run(case)
+    pkv.decode_set_chunks_per_split(chunks)
+    got = gpu_run(case)
+    assert got["flags"] == 0
+    assert_close(got["out"], got["lse"], ref["out"], ref["lse"], f"chunks={chunks}")
+
+
+@pytest.mark.parametrize("kind", ["decode", "prefill"])
+def test_block_relabelling_is_bit_identical(kind):
+    case = SMALL["tiny/decode" if kind == "decode" else "tiny/prefill"]
+    got = gpu_run(case)
+    kc = host_u16(got["kc"])
+    vc = host_u16(got["vc"])
+    relabel = np.random.default_rng(1).permutation(case.num_blocks).astype(np.int32)
+    kc2, vc2 = np.empty_like(kc), np.empty_like(vc)
+    kc2[relabel] = kc
+    vc2[relabel] = vc
+    bt2 = np.where(case.block_tables >= 0, relabel[np.maximum(case.block_tables, 0)], -1)
+    case2 = dataclasses.replace(case, block_tables=bt2.astype(np.int32))
+    out2, lse2 = gpu_attend(case2, dev_bf16(kc2), dev_bf16(vc2))
+    assert np.array_equal(out2.double().cpu().numpy(), got["out"])
+    assert np.array_equal(lse2.double().cpu().numpy(), got["lse"])
+
+
+def test_decode_matches_last_prefill_row():
+    n = 300
+    pre = W.prefill_case("p300", 21, [n], [n], block_size=16, num_blocks=20, blocks_per_seq=20)
+    got = gpu_run(pre)
+    for t in (0, 127, 128, 255, n - 1):
+        out_d, lse_d = pkv.paged_decode_attn(
+            dev_bf16(pre.step.q[t:t + 1]), got["kc"], got["vc"], dev_i32(pre.block_tables),
+            dev_i32(np.array([t + 1], np.int32)), t + 1, pre.scale)
+        assert np.abs(out_d.double().cpu().numpy()[0] - got["out"][t]).max() <= 2 * 2e-2
+        assert np.abs(lse_d.double().cpu().numpy()[0] - got["lse"][t]).max() <= 2e-3
+
+
+# ---------------------------------------------------------------- edge cases
+
+def _check_case(case):
+    got = gpu_run(case)
+    ref = oracle_run(case)
+    assert got["flags"] == 0
+    assert_cache_equal(got["kc"], got["vc"], ref["kc"], ref["vc"])
+    return assert_close(got["out"], got["lse"], ref["out"], ref["lse"], case.name)
+
+
+def test_decode_single_key_and_block_edges():
+    # contexts 1, 15, 16, 17, 31, 32, 33 with block size 16
+    _check_case(W.decode_case("edges", 31, [1, 15, 16, 17, 31, 32, 33], block_size=16,
+                              num_blocks=40, blocks_per_seq=3))
+
+
+def test_decode_long_context_mixed():
+    _check_case(W.decode_case("long", 32, [32768, 5, 4097, 1000], block_size=256,
+                              num_blocks=4 * 128, blocks_per_seq=128))
+
+
+@pytest.mark.parametrize("h_q,h_kv", [(8, 8), (32, 8), (4, 2)])
+def test_decode_other_gqa_groups(h_q, h_kv):
+    _check_case(W.decode_case(f"gqa{h_q}x{h_kv}", 33, [77, 300, 1], block_size=32, num_blocks=30,
+                              blocks_per_seq=10, H_q=h_q, H_kv=h_kv))
+
+
+@pytest.mark.parametrize("h_q,h_kv", [(8, 8), (32, 8)])
+def test_prefill_other_gqa_groups(h_q, h_kv):
+    _check_case(W.prefill_case(f"pgqa{h_q}x{h_kv}", 34, [130, 7], [200, 7], block_size=64,
+                               num_blocks=8, blocks_per_seq=4, H_q=h_q, H_kv=h_kv))
+
+
+def test_prefill_ragged_prefix_empty_and_single_rows():
+    # empty segment, single-token prompt over a prefix, unaligned prefix, block size 16
+    _check_case(W.prefill_case("ragged", 35, q_lens=[1, 0, 129, 255, 40],
+                               k_lens=[1, 30, 129 + 19, 300, 40 + 200], block_size=16,
+                               num_blocks=5 * 20, blocks_per_seq=20))
+
+
+def test_prefill_block_sizes():
+    for bs in (32, 48, 128):
+        _check_case(W.prefill_case(f"bs{bs}", 36 + bs, [70, 260], [90, 260], block_size=bs,
+                                   num_blocks=2 * (300 // bs + 1), blocks_per_seq=300 // bs + 1))
+
+
+def test_kv_store_minus_one_and_empty():
+    case = SMALL["tiny/decode"]
+    kc, vc = gpu_pool(case)
+    st = case.step.new
+    slots = st.slots.copy()
+    slots[1] = -1
+    pkv.kv_store(dev_bf16(st.k), dev_bf16(st.v), kc, vc, dev_i32(slots))
+    empty = np.zeros((0, case.H_kv, case.D), np.uint16)
+    pkv.kv_store(dev_bf16(empty), dev_bf16(empty), kc, vc, dev_i32(np.zeros(0, np.int32)))
+    assert pkv.check_device_errors() == 0
+    rk, rv = case.poisoned_pool(), case.poisoned_pool()
+    oracle.kv_store(st.k, st.v, rk, rv, slots)
+    assert_cache_equal(kc, vc, rk, rv)
+
+
+# ---------------------------------------------------------------- device-side checks
+
+def test_out_of_range_slot_is_skipped_and_flagged():
+    case = SMALL["tiny/decode"]
+    kc, vc = gpu_pool(case)
+    st = case.step.new
+    slots = st.slots.copy()
+    slots[2] = case.num_blocks * case.block_size  # one past the pool
+    pkv.kv_store(dev_bf16(st.k), dev_bf16(st.v), kc, vc, dev_i32(slots))
+    assert pkv.check_device_errors() & pkv.DEVERR_SLOT
+    rk, rv = case.poisoned_pool(), case.poisoned_pool()
+    ok = slots.copy()
+    ok[2] = -1
+    oracle.kv_store(st.k, st.v, rk, rv, ok)
+    assert_cache_equal(kc, vc, rk, rv)
+    assert pkv.check_device_errors() == 0  # reading clears the word
+
+
+def test_bad_block_entry_and_context_are_flagged():
+    case = SMALL["tiny/decode"]
+    got = gpu_run(case)
+    bt = case.block_tables.copy()
+    bt[2, 0] = case.num_blocks  # outside the pool
+    pkv.paged_decode_attn(dev_bf16(case.step.q), got["kc"], got["vc"], dev_i32(bt),
+                          dev_i32(case.step.context_lens), case.step.max_context_len, case.scale)
+    assert pkv.check_device_errors() & pkv.DEVERR_BLOCK
+    ctx = case.step.context_lens.copy()
+    ctx[0] = 0
+    pkv.paged_decode_attn(dev_bf16(case.step.q), got["kc"], got["vc"],
+                          dev_i32(case.block_tables), dev_i32(ctx), case.step.max_context_len,
+                          case.scale)
+    assert pkv.check_device_errors() & pkv.DEVERR_CONTEXT
+
+
+def test_prefill_bad_seqlens_are_flagged():
+    case = SMALL["tiny/prefill"]
+    got = gpu_run(case)
+    st = case.step
+    # claim a smaller maximum than the real prompt lengths
+    pkv.paged_prefill_attn(dev_bf16(st.q), got["kc"], got["vc"], dev_i32(st.cu_seqlens_q),
+                           dev_i32(st.cu_seqlens_k), dev_i32(case.block_tables), 32, 64,
+                           case.scale)
+    assert pkv.check_device_errors() & pkv.DEVERR_SEQLENS
