@@ -128,6 +128,11 @@ __global__ void __launch_bounds__(NW * 32)
   const int warp = threadIdx.x >> 5;
   const int j = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
 
+  // a CTA gave up waiting (in this or an earlier launch): skip the work until
+  // the error word is read and cleared; decided once per CTA
+  if (__syncthreads_or(threadIdx.x == 0 &&
+                       (*reinterpret_cast<volatile uint32_t *>(&g_decode_errors) & kErrTimeout)))
+    return;
   const int ctx = p.context_lens[s];
   if (ctx <= 0 || ctx > p.max_context_len ||
       static_cast<int64_t>(ctx) > static_cast<int64_t>(p.max_blocks) * p.block_size) {
@@ -198,7 +203,7 @@ __global__ void __launch_bounds__(NW * 32)
   for (int it = 0; it < mine; ++it) {
     const int st = it % NS;
     const uint32_t stage = stage0 + st * kStageBytes;
-    const bool landed = mbar_wait(bar0 + 8 * st, (it / NS) & 1);
+    const bool landed = mbar_wait(bar0 + 8 * st, (it / NS) & 1, &g_decode_errors);
     if (!__all_sync(0xffffffffu, landed)) {
       if (lane == 0) atomicOr(&g_decode_errors, kErrTimeout);
       ok = false;

@@ -62,6 +62,10 @@ struct PrefillParams {
   float scale_log2;
 };
 
+__device__ __forceinline__ bool wait_(uint32_t bar, uint32_t parity, const volatile int *abort) {
+  return mbar_wait(bar, parity, &g_prefill_errors, abort);
+}
+
 __device__ __forceinline__ void fail(volatile int *abort) {
   *abort = 1;
   atomicOr(&g_prefill_errors, kErrTimeout);
@@ -78,6 +82,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t = p.n_qtiles - 1 - static_cast<int>(blockIdx.x);  // heaviest tiles first
   const int h = blockIdx.y, s = blockIdx.z;
   const int g = h / (p.num_q_heads / p.num_kv_heads);
+
+  // a CTA gave up waiting (in this or an earlier launch): skip the work until
+  // the error word is read and cleared; decided once per CTA
+  if (__syncthreads_or(tid == 0 &&
+                       (*reinterpret_cast<volatile uint32_t *>(&g_prefill_errors) & kErrTimeout)))
+    return;
 
   const int q0 = p.cu_q[s], q1 = p.cu_q[s + 1];
   const int Lq = q1 - q0, Lk = p.cu_k[s + 1] - p.cu_k[s];
@@ -135,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t table = static_cast<int64_t>(s) * p.max_blocks;
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j & 1;
-        if (j >= kStages && !mbar_wait_or_abort(bar(kBarKvEmpty + st), ((j >> 1) - 1) & 1, abort)) {
+        if (j >= kStages && !wait_(bar(kBarKvEmpty + st), ((j >> 1) - 1) & 1, abort)) {
           fail(abort);
           break;
         }
@@ -177,10 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    bool good = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(kBarQ), 0, abort));
+    bool good = __all_sync(0xffffffffu, wait_(bar(kBarQ), 0, abort));
     auto issue_s = [&](int j) -> bool {
       const int st = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bar(kBarKFull + st), (j >> 1) & 1, abort)))
+      if (!__all_sync(0xffffffffu, wait_(bar(kBarKFull + st), (j >> 1) & 1, abort)))
         return false;
       tc_fence_after();
       if (lane == 0) {
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto issue_pv = [&](int j) -> bool {
       const int st = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bar(kBarVFull + st), (j >> 1) & 1, abort)))
+      if (!__all_sync(0xffffffffu, wait_(bar(kBarVFull + st), (j >> 1) & 1, abort)))
         return false;
       const int r0 = Lk - j * kBN;  // V rows >= r0 are past the segment's last key
       if (r0 < kBN) {
@@ -230,11 +240,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (good) good = issue_s(0);
     for (int j = 1; good && j < n_tiles; ++j) {
-      good = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(kBarP), (j - 1) & 1, abort)) &&
+      good = __all_sync(0xffffffffu, wait_(bar(kBarP), (j - 1) & 1, abort)) &&
              issue_s(j) && issue_pv(j - 1);
     }
     if (good)
-      good = __all_sync(0xffffffffu, mbar_wait_or_abort(bar(kBarP), (n_tiles - 1) & 1, abort)) &&
+      good = __all_sync(0xffffffffu, wait_(bar(kBarP), (n_tiles - 1) & 1, abort)) &&
              issue_pv(n_tiles - 1);
     if (!good && lane == 0) fail(abort);
   } else {
@@ -247,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool good = true;
     uint32_t x[kBN];
     for (int j = 0; j < n_tiles; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bar(kBarS), j & 1, abort))) {
+      if (!__all_sync(0xffffffffu, wait_(bar(kBarS), j & 1, abort))) {
         good = false;
         break;
       }
@@ -280,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j > 0) {
         // P.V of the previous tile must be done: it reads the P buffer and
         // accumulates into the O row that is rescaled here
-        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(bar(kBarO), (j - 1) & 1, abort))) {
+        if (!__all_sync(0xffffffffu, wait_(bar(kBarO), (j - 1) & 1, abort))) {
           good = false;
           break;
         }
@@ -314,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(kBarP));
     }
-    if (__all_sync(0xffffffffu, good && mbar_wait_or_abort(bar(kBarO), (n_tiles - 1) & 1, abort))) {
+    if (__all_sync(0xffffffffu, good && wait_(bar(kBarO), (n_tiles - 1) & 1, abort))) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool store = qi < Lq;

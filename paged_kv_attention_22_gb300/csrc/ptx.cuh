@@ -1,7 +1,7 @@
 // Inline-PTX building blocks for sm_103a: mbarriers, TMA tensor copies and
 // tcgen05 (5th-generation tensor core) MMA with TMEM accumulators.
 //
-// Every wait is bounded: mbar_wait gives up after kWaitLimit polls and returns
+// Every wait is bounded: mbar_wait gives up after a wall-time limit and returns
 // false, so a kernel that never receives an arrival reports an error instead of
 // hanging the GPU.
 #pragma once
@@ -19,12 +19,18 @@ constexpr uint32_t kErrContext = 0x4u;
 constexpr uint32_t kErrSeqlens = 0x8u;
 constexpr uint32_t kErrTimeout = 0x10u;
 
-// try_wait suspends for a hardware-defined slice per poll; 2^24 polls is far
-// beyond any legitimate wait (microseconds) and still ends within seconds.
-constexpr uint32_t kWaitLimit = 1u << 24;
+// A wait gives up after kWaitTimeoutNs of wall time (%globaltimer). Correct
+// waits take microseconds; the limit only turns a lost arrival into an error.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
 
 // ---------------------------------------------------------------- mbarrier
@@ -59,26 +65,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Wait for the phase with the given parity to complete. Returns false if the
-// poll limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete. Returns false when the
+// wall-time limit runs out, when the kernel's error word already holds
+// kErrTimeout (another CTA gave up: stop early instead of timing out one CTA
+// after another), or when *cta_abort (if given) is set by another role of
+// this CTA.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          const volatile uint32_t *kernel_errors,
+                                          const volatile int *cta_abort = nullptr) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
 #pragma unroll 1
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (cta_abort != nullptr && *cta_abort) return false;
+      if (*kernel_errors & kErrTimeout) return false;
+      if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
   }
-  return false;
-}
-
-// Same, but also gives up early when *abort becomes non-zero (another role of
-// the CTA already timed out).
-__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity,
-                                                   const volatile int *abort) {
-#pragma unroll 1
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 63u && *abort) return false;
-  }
-  return false;
 }
 
 // ---------------------------------------------------------------- proxies
