@@ -220,14 +220,14 @@ def _dev(a):
 
 
 class Sweep:
-    """The 28 layers' device state and pre-marshalled C-ABI calls."""
+    """The layers' device state and pre-marshalled C-ABI calls."""
 
-    def __init__(self, pkv, seed_base):
+    def __init__(self, pkv, seed_base, num_layers=LAYERS):
         self.pkv = pkv
         self.L = pkv.lib()
         self.layers = []
         self.host_cases = []
-        for layer in range(LAYERS):
+        for layer in range(num_layers):
             case = W.sweep64_layer(layer, base_seed=seed_base)
             kc, vc = _dev(case.poisoned_pool()), _dev(case.poisoned_pool())
             pkv.kv_store(_dev(case.history.k), _dev(case.history.v), kc, vc,
@@ -291,7 +291,7 @@ def time_sweep(sweep, steps, warmup, device):
         sweep.run_step(calls)
     torch.cuda.synchronize()
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(LAYERS)] for _ in range(steps)]
+           for _ in range(len(sweep.layers))] for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
@@ -492,6 +492,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the decode sweep (profiling the prefill leg alone)")
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="layers per step (28 for the real workload; fewer for profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -519,33 +523,49 @@ def main(argv=None):
                "sample": desc}
 
     peaks = load_peaks()
-    sweep = Sweep(pkv, seed_base=4000 + 1000 * rank)
-    with ClockSampler(local) as clocks:
-        total_ms, decode_ms = time_sweep(sweep, args.steps, args.warmup, local)
-    graph_ms = time_sweep_graph(sweep, args.steps, args.warmup)
-    if pkv.check_device_errors() != 0:
-        raise RuntimeError("device error during the timed region")
-
-    t_max = max_over_ranks(total_ms / 1000.0, device="cuda")
-    g_max = max_over_ranks(graph_ms / 1000.0, device="cuda")
-    units = sum_over_ranks(args.steps * LAYERS * DECODE_SEQS, device="cuda")
-    value_eager = units / t_max
-    value_graph = units / g_max
-
-    dec_bytes = decode_algorithmic_bytes(DECODE_SEQS, DECODE_CTX)
-    dec_s = statistics.mean(decode_ms) / 1000.0
-    achieved = dec_bytes / dec_s / 1e9
-    digest = source_digest("decode.cu", "ptx.cuh")
-    traffic = profiled_traffic("decode_split", digest)
-
+    layers = args.layers
+    value_graph = value_eager = t_max = g_max = None
+    roofline = None
     e2e = None
-    if not args.no_e2e:
-        e_ms, h2d, d2h = time_e2e(sweep, max(args.steps // 4, 10), args.warmup)
-        n_e2e = max(args.steps // 4, 10)
-        e_max = max_over_ranks(e_ms / 1000.0, device="cuda")
-        e_units = sum_over_ranks(n_e2e * LAYERS * DECODE_SEQS, device="cuda")
-        e2e = {"value": e_units / e_max, "unit": "seq·layer/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "path": "python API, pinned host buffers"}
+    clocks_result = None
+    launches_per_step = 0
+    splits = None
+    if not args.no_sweep:
+        sweep = Sweep(pkv, seed_base=4000 + 1000 * rank, num_layers=layers)
+        splits = sweep.num_splits
+        with ClockSampler(local) as clocks:
+            total_ms, decode_ms = time_sweep(sweep, args.steps, args.warmup, local)
+        clocks_result = clocks.result
+        graph_ms = time_sweep_graph(sweep, args.steps, args.warmup)
+        if pkv.check_device_errors() != 0:
+            raise RuntimeError("device error during the timed region")
+        t_max = max_over_ranks(total_ms / 1000.0, device="cuda")
+        g_max = max_over_ranks(graph_ms / 1000.0, device="cuda")
+        units = sum_over_ranks(args.steps * layers * DECODE_SEQS, device="cuda")
+        value_eager = units / t_max
+        value_graph = units / g_max
+        dec_bytes = decode_algorithmic_bytes(DECODE_SEQS, DECODE_CTX)
+        dec_s = statistics.mean(decode_ms) / 1000.0
+        achieved = dec_bytes / dec_s / 1e9
+        digest = source_digest("decode.cu", "ptx.cuh")
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                    "traffic": profiled_traffic("decode_split", digest),
+                    "kernel": "decode call (split + merge)",
+                    "algorithmic_bytes_per_launch": dec_bytes,
+                    "us_per_launch": dec_s * 1e6,
+                    "peak_kind": f"HBM copy ({peaks['source']})",
+                    "source_digest": digest}
+        launches_per_step = layers * (2 + (1 if splits > 1 else 0))
+        if not args.no_e2e:
+            n_e2e = max(args.steps // 4, 10)
+            e_ms, h2d, d2h = time_e2e(sweep, n_e2e, args.warmup)
+            e_max = max_over_ranks(e_ms / 1000.0, device="cuda")
+            e_units = sum_over_ranks(n_e2e * layers * DECODE_SEQS, device="cuda")
+            e2e = {"value": e_units / e_max, "unit": "seq·layer/s", "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h, "path": "python API, pinned host buffers"}
+        del sweep
+        torch.cuda.empty_cache()
 
     prefill = None
     if not args.no_prefill:
@@ -562,7 +582,6 @@ def main(argv=None):
                    "kv_store_frac": store_gbs / peaks["hbm_gbs"],
                    "kv_store_tokens": 32768}
 
-    launches_per_step = LAYERS * (2 + (1 if sweep.num_splits > 1 else 0))
     if rank == 0:
         line = {
             "metric": METRIC,
@@ -571,31 +590,27 @@ def main(argv=None):
             "n_gpus": world,
             "steps": args.steps,
             "warmup": args.warmup,
-            "ms_per_step": 1000.0 * g_max / args.steps,
+            "ms_per_step": 1000.0 * g_max / args.steps if g_max else None,
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": "decode sweep c=64: 64 seqs x ctx 640, 28 distinct layer "
-                                   "caches, bs=256, 16 q / 8 kv heads x 128, KV store + decode "
-                                   "per layer",
+            "config": {"workload": f"decode sweep c=64: 64 seqs x ctx 640, {layers} distinct "
+                                   "layer caches, bs=256, 16 q / 8 kv heads x 128, KV store + "
+                                   "decode per layer",
                        "timing": "CUDA graph of one step, replayed",
-                       "l2": "inputs larger than L2 (4.7 GB of K/V per step)",
-                       "decode_splits": sweep.num_splits},
-            "eager": {"value": value_eager, "ms_per_step": 1000.0 * t_max / args.steps},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": traffic,
-                         "kernel": "decode call (split + merge)",
-                         "algorithmic_bytes_per_launch": dec_bytes,
-                         "us_per_launch": dec_s * 1e6,
-                         "peak_kind": f"HBM copy ({peaks['source']})"},
+                       "l2": f"inputs larger than L2 ({layers * 168.3 / 1000:.1f} GB of K/V per "
+                             "step, 168 MB per layer)",
+                       "decode_splits": splits},
+            "eager": ({"value": value_eager, "ms_per_step": 1000.0 * t_max / args.steps}
+                      if t_max else None),
+            "roofline": roofline,
             "prefill": prefill,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks.result,
+            "clocks": clocks_result,
         }
         print(json.dumps(line))
     if torch.distributed.is_initialized():
