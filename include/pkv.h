@@ -152,6 +152,38 @@ int32_t pkv_decode_num_splits(int32_t num_seqs, int32_t num_q_heads, int32_t num
 void pkv_decode_set_chunks_per_split(int32_t chunks);
 
 /*
+ * Decode attention for callers that cannot allocate device memory.
+ * (An addition of this library: the pages have no counterpart.)
+ * Some callers of decode cannot call cudaMalloc where they run: a plugin inside
+ * a host framework whose allocator owns the whole device pool, a deployment
+ * that forbids dynamic allocation after start-up, a latency-critical loop where
+ * an allocation may synchronise the device. This call computes exactly what
+ * pkv_paged_decode_attn computes, with the same arguments except the
+ * workspace: its scratch is a static device array of
+ * PKV_DECODE_NOALLOC_SCRATCH_BYTES inside libpkv.so, present on every GPU that
+ * loads the library until the process exits. It calls no cudaMalloc, cudaFree
+ * or other allocator.
+ *   - Sizes whose pkv_decode_workspace_size exceeds that limit are rejected with
+ *     PKV_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares that device's one array, which keeps the
+ *     last call's contents; nothing in it needs to start at zero. Calls that
+ *     can overlap on the GPU (for example on two streams with no ordering
+ *     between them) race on the array: the caller must order them.
+ */
+#define PKV_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
+pkv_status pkv_paged_decode_attn_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                         const int32_t *block_tables,
+                                         int32_t max_blocks_per_seq,
+                                         const int32_t *context_lens, int32_t max_context_len,
+                                         int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t block_size, int64_t num_blocks, float scale,
+                                         void *out, float *lse, void *stream);
+
+/*
  * Bytes of device workspace that pkv_paged_prefill_attn needs (currently 0 for
  * every size: the prefill kernel keeps all its state on chip).
  */

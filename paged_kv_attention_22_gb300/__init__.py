@@ -70,6 +70,9 @@ def lib():
     L.pkv_paged_decode_attn.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64,
                                         f32, P, P, P, sz, P]
     L.pkv_paged_decode_attn.restype = ctypes.c_int
+    L.pkv_paged_decode_attn_noalloc.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32,
+                                                i32, i64, f32, P, P, P]
+    L.pkv_paged_decode_attn_noalloc.restype = ctypes.c_int
     L.pkv_decode_num_splits.argtypes = [i32, i32, i32, i32, i32]
     L.pkv_decode_num_splits.restype = i32
     L.pkv_decode_set_chunks_per_split.argtypes = [i32]
@@ -176,6 +179,33 @@ def paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, max_conte
         _ptr(context_lens), int(max_context_len), S, H_q, H_kv, D, bs, NB, float(scale),
         _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)),
         "pkv_paged_decode_attn")
+    return out, lse
+
+
+# Static scratch of paged_decode_attn_noalloc (PKV_DECODE_NOALLOC_SCRATCH_BYTES).
+DECODE_NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def paged_decode_attn_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                              scale, out, lse=None, stream=None):
+    """Decode attention for callers that cannot allocate device memory: same
+    result as paged_decode_attn, with the library's static scratch in place of a
+    workspace. `out` (and `lse`, if wanted) must be supplied; nothing is
+    allocated here either. Calls overlapping on one GPU race on the scratch."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    S, H_q, D = q.shape
+    NB, bs, H_kv, _ = k_cache.shape
+    _check(lib().pkv_paged_decode_attn_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), int(max_context_len), S, H_q, H_kv, D, bs, NB, float(scale),
+        _ptr(out), _ptr(lse), _stream(stream)), "pkv_paged_decode_attn_noalloc")
     return out, lse
 
 

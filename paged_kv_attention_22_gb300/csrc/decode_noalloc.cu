@@ -1,0 +1,63 @@
+// Paged decode attention without a caller-supplied workspace.
+//
+// The split-K decode call needs scratch memory for its per-split partial
+// results. pkv_paged_decode_attn takes that scratch from the caller. Some
+// callers cannot allocate device memory where they run: a plugin inside a host
+// framework whose allocator owns the whole device pool and refuses foreign
+// allocations, a deployment that forbids dynamic allocation after start-up, or
+// a latency-critical loop where cudaMalloc/cudaFree may synchronise the device.
+// This entry point serves them from a fixed array of static device memory that
+// belongs to this file, so it calls no allocator at all.
+#include <mutex>
+
+#include "../../include/pkv.h"
+#include "internal.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = PKV_DECODE_NOALLOC_SCRATCH_BYTES;
+
+// Present on every GPU that loads this library, for the life of the process.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once per
+// device. In host code the array's name is only a host-side stand-in, so the
+// kernels must be given this address, never the name.
+pkv_status scratch_for_current_device(void **ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return PKV_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *ptr = g_scratch_ptr[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" pkv_status pkv_paged_decode_attn_noalloc(
+    const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
+    int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t max_context_len,
+    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int64_t num_blocks, float scale, void *out, float *lse, void *stream) {
+  const size_t need = pkv_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len);
+  if (need == 0) return PKV_ERR_INVALID_ARG;
+  if (need > kScratchBytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  void *scratch = nullptr;
+  const pkv_status st = scratch_for_current_device(&scratch);
+  if (st != PKV_OK) return st;
+  // Nothing in the scratch has to start at zero: each call writes every partial
+  // result it reads back.
+  return pkv_paged_decode_attn(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                               max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                               block_size, num_blocks, scale, out, lse, scratch, kScratchBytes,
+                               stream);
+}
