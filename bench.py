@@ -239,7 +239,8 @@ class Sweep:
                      ctx=_dev(st.context_lens), out=torch.empty((S, H_q, D), dtype=torch.bfloat16,
                                                                  device="cuda"),
                      lse=torch.empty((S, H_q), dtype=torch.float32, device="cuda"))
-            d["ws"] = torch.empty(pkv.decode_workspace_size(S, H_q, D, st.max_context_len),
+            d["ws"] = torch.empty(pkv.decode_workspace_size(S, H_q, case.H_kv, D,
+                                                            st.max_context_len),
                                   dtype=torch.uint8, device="cuda")
             self.layers.append(d)
             self.host_cases.append(case)
@@ -250,7 +251,6 @@ class Sweep:
         self.S, self.H_q, self.D = c0.step.q.shape
         self.H_kv, self.bs, self.NB = c0.H_kv, c0.block_size, c0.num_blocks
         self.max_ctx = c0.step.max_context_len
-        self.num_splits = pkv.decode_num_splits(self.S, self.H_q, self.H_kv, self.D, self.max_ctx)
         self.scale = c0.scale
 
     def calls(self, stream_handle):
@@ -494,6 +494,10 @@ def main(argv=None):
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the decode sweep (profiling the prefill leg alone)")
+    ap.add_argument("--decode-ctas", type=int, default=0,
+                    help="persistent decode CTAs (0: one per SM)")
+    ap.add_argument("--decode-variant", type=int, default=0,
+                    help="decode launch shape (warps per CTA x stages per warp)")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layers per step (28 for the real workload; fewer for profiling)")
     args = ap.parse_args(argv)
@@ -514,6 +518,7 @@ def main(argv=None):
         pkv_build.build()
     barrier()
     pkv.lib()
+    pkv.decode_set_config(args.decode_ctas, args.decode_variant)
 
     # CPU baseline before any heavy GPU work (rank 0, N=1 only)
     cpu = None
@@ -529,10 +534,8 @@ def main(argv=None):
     e2e = None
     clocks_result = None
     launches_per_step = 0
-    splits = None
     if not args.no_sweep:
         sweep = Sweep(pkv, seed_base=4000 + 1000 * rank, num_layers=layers)
-        splits = sweep.num_splits
         with ClockSampler(local) as clocks:
             total_ms, decode_ms = time_sweep(sweep, args.steps, args.warmup, local)
         clocks_result = clocks.result
@@ -551,12 +554,12 @@ def main(argv=None):
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                     "traffic": profiled_traffic("decode_split", digest),
-                    "kernel": "decode call (split + merge)",
+                    "kernel": "decode_kernel (persistent split-K with in-kernel merge)",
                     "algorithmic_bytes_per_launch": dec_bytes,
                     "us_per_launch": dec_s * 1e6,
                     "peak_kind": f"HBM copy ({peaks['source']})",
                     "source_digest": digest}
-        launches_per_step = layers * (2 + (1 if splits > 1 else 0))
+        launches_per_step = layers * 2  # KV store + decode (plus a counter memset)
         if not args.no_e2e:
             n_e2e = max(args.steps // 4, 10)
             e_ms, h2d, d2h = time_e2e(sweep, n_e2e, args.warmup)
@@ -602,7 +605,8 @@ def main(argv=None):
                        "timing": "CUDA graph of one step, replayed",
                        "l2": f"inputs larger than L2 ({layers * 168.3 / 1000:.1f} GB of K/V per "
                              "step, 168 MB per layer)",
-                       "decode_splits": splits},
+                       "decode": "persistent split-K, one CTA per SM",
+                       "decode_ctas": args.decode_ctas, "decode_variant": args.decode_variant},
             "eager": ({"value": value_eager, "ms_per_step": 1000.0 * t_max / args.steps}
                       if t_max else None),
             "roofline": roofline,

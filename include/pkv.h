@@ -101,13 +101,17 @@ pkv_status pkv_kv_store(const void *k, const void *v, void *k_cache, void *v_cac
                         int64_t num_blocks, void *stream);
 
 /*
- * Bytes of device workspace that pkv_paged_decode_attn needs for these sizes
- * (0 on invalid sizes). The workspace holds the per-split partial results of
- * the split-K kernel; the caller allocates it once and may reuse it for every
- * call with sizes no larger than these.
+ * Bytes of device workspace that pkv_paged_decode_attn needs for these sizes on
+ * the current device (0 on invalid sizes or without a device). The workspace
+ * holds per-pair arrival counters and the partial results of pairs whose keys
+ * are split between warps; its size depends on the number of sequences and
+ * heads and on the device's SM count, not on context length. The caller
+ * allocates it once and may reuse it for every call with sizes no larger than
+ * these; it needs no initialisation (the counters are zeroed on the stream by
+ * every call).
  */
-size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
-                                 int32_t max_context_len);
+size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_context_len);
 
 /*
  * Paged decode attention, one query token per sequence (q=1 decode).
@@ -126,6 +130,7 @@ size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t 
  *   out            device bf16 [num_seqs, num_q_heads, head_dim]
  *   lse            device float32 [num_seqs, num_q_heads], or NULL
  *   workspace      device, >= pkv_decode_workspace_size(...) bytes, 16-byte aligned
+ * num_seqs is at most 2048.
  * Rows whose context_len is invalid raise PKV_DEVERR_CONTEXT and are not written.
  */
 pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
@@ -137,19 +142,13 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
                                  size_t workspace_bytes, void *stream);
 
 /*
- * Number of splits (partial results per query row) that pkv_paged_decode_attn
- * uses for these sizes on the current device; 1 means the merge kernel is not
- * launched. Returns -1 on invalid sizes or a CUDA error.
+ * Tuning knob of the decode launch, process-wide (not thread-safe against
+ * concurrent launches): ctas = number of persistent CTAs (0 = one per SM, the
+ * default); variant = launch shape (0 = default; 1..3 trade warps per CTA for
+ * TMA stages per warp). Results do not depend on either, beyond rounding.
+ * A non-default ctas changes pkv_decode_workspace_size.
  */
-int32_t pkv_decode_num_splits(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                              int32_t head_dim, int32_t max_context_len);
-
-/*
- * Tuning knob of the decode kernel: the number of 32-key chunks per split
- * (0 = automatic, the default). Process-wide; not thread-safe against
- * concurrent launches. Values are clamped to [2, 1024].
- */
-void pkv_decode_set_chunks_per_split(int32_t chunks);
+void pkv_decode_set_config(int32_t ctas, int32_t variant);
 
 /*
  * Decode attention for callers that cannot allocate device memory.

@@ -65,7 +65,7 @@ def lib():
     L.pkv_last_cuda_error.restype = ctypes.c_char_p
     L.pkv_kv_store.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i64, P]
     L.pkv_kv_store.restype = ctypes.c_int
-    L.pkv_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+    L.pkv_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.pkv_decode_workspace_size.restype = sz
     L.pkv_paged_decode_attn.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64,
                                         f32, P, P, P, sz, P]
@@ -73,10 +73,8 @@ def lib():
     L.pkv_paged_decode_attn_noalloc.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32,
                                                 i32, i64, f32, P, P, P]
     L.pkv_paged_decode_attn_noalloc.restype = ctypes.c_int
-    L.pkv_decode_num_splits.argtypes = [i32, i32, i32, i32, i32]
-    L.pkv_decode_num_splits.restype = i32
-    L.pkv_decode_set_chunks_per_split.argtypes = [i32]
-    L.pkv_decode_set_chunks_per_split.restype = None
+    L.pkv_decode_set_config.argtypes = [i32, i32]
+    L.pkv_decode_set_config.restype = None
     L.pkv_prefill_workspace_size.argtypes = [i32, i32]
     L.pkv_prefill_workspace_size.restype = sz
     L.pkv_paged_prefill_attn.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
@@ -135,22 +133,19 @@ def kv_store(k, v, k_cache, v_cache, slot_mapping, stream=None):
                               k.shape[0], H_kv, D, bs, NB, _stream(stream)), "pkv_kv_store")
 
 
-def decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len) -> int:
-    return int(lib().pkv_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len))
+def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len) -> int:
+    """Workspace bytes of paged_decode_attn on the current device (0: invalid sizes)."""
+    return int(lib().pkv_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                               max_context_len))
 
 
-def decode_num_splits(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len) -> int:
-    """Splits the decode call would use on the current device (1: no merge kernel)."""
-    n = int(lib().pkv_decode_num_splits(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                        max_context_len))
-    if n < 0:
-        raise PkvError(PKV_ERR_CUDA, "pkv_decode_num_splits")
-    return n
+DECODE_NUM_VARIANTS = 4
 
 
-def decode_set_chunks_per_split(chunks: int) -> None:
-    """Tuning knob: 32-key chunks per decode split (0 = automatic)."""
-    lib().pkv_decode_set_chunks_per_split(int(chunks))
+def decode_set_config(ctas: int = 0, variant: int = 0) -> None:
+    """Tuning knob of the decode launch: persistent CTAs (0 = one per SM) and
+    launch-shape variant (0 = default). Process-wide."""
+    lib().pkv_decode_set_config(int(ctas), int(variant))
 
 
 def paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
@@ -170,7 +165,7 @@ def paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, max_conte
         lse = torch.empty((S, H_q), dtype=torch.float32, device=q.device)
     if lse is not None:
         _need(lse, "lse", torch.float32, 2)
-    need = decode_workspace_size(S, H_q, D, int(max_context_len))
+    need = decode_workspace_size(S, H_q, H_kv, D, int(max_context_len))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     _need(workspace, "workspace", torch.uint8, 1)

@@ -79,9 +79,10 @@ pkv_status get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn) {
 }
 
 // A 3-D bf16 view [rows, heads, dim] (dim innermost, contiguous) with a box of
-// box_dim x 1 head x box_rows rows.
+// box_dim x box_heads x box_rows.
 pkv_status encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int32_t heads,
-                           int32_t dim, uint32_t box_dim, uint32_t box_rows, bool swizzle128) {
+                           int32_t dim, uint32_t box_dim, uint32_t box_heads, uint32_t box_rows,
+                           bool swizzle128) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   pkv_status st = get_encoder(&enc);
   if (st != PKV_OK) return st;
@@ -89,7 +90,7 @@ pkv_status encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int
                         static_cast<cuuint64_t>(rows)};
   cuuint64_t gstride[2] = {static_cast<cuuint64_t>(dim) * 2,
                            static_cast<cuuint64_t>(dim) * 2 * static_cast<cuuint64_t>(heads)};
-  cuuint32_t box[3] = {box_dim, 1, box_rows};
+  cuuint32_t box[3] = {box_dim, box_heads, box_rows};
   cuuint32_t estride[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), gdim,
                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -101,7 +102,9 @@ pkv_status encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-std::atomic<int32_t> g_decode_chunks_override{0};
+// Tuning overrides of the decode launch (0 = automatic / default).
+std::atomic<int32_t> g_decode_ctas{0};
+std::atomic<int32_t> g_decode_variant{0};
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -125,21 +128,29 @@ pkv_status check_attention_shape(int32_t num_q_heads, int32_t num_kv_heads, int3
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Decode workspace layout: lse partials first, then output partials, both
-// sized for the largest split count any plan can choose.
+// Decode workspace layout: arrival counters [S * H_kv], then per-warp partial
+// (max, sum) [2W, G, 2] and partial outputs [2W, G, D], for W = grid warps of
+// the widest launch variant.
 struct DecodeWorkspace {
-  size_t lse_bytes, o_offset, total;
+  size_t cnt_bytes, ml_offset, o_offset, total;
 };
 
-bool decode_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
-                             int32_t max_context_len, DecodeWorkspace *w) {
-  if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len <= 0) return false;
-  const int64_t min_keys = static_cast<int64_t>(pkv::kDecodeChunk) * pkv::kDecodeMinChunksPerSplit;
-  const int64_t j_max = (max_context_len + min_keys - 1) / min_keys;
-  const int64_t rows = static_cast<int64_t>(num_seqs) * num_q_heads;
-  w->lse_bytes = static_cast<size_t>(rows * j_max) * sizeof(float);
-  w->o_offset = align_up(w->lse_bytes, 256);
-  w->total = w->o_offset + static_cast<size_t>(rows * j_max * head_dim) * sizeof(float);
+int32_t decode_grid_ctas(int sms) {
+  const int32_t o = g_decode_ctas.load(std::memory_order_relaxed);
+  return o > 0 ? (o > 65535 ? 65535 : o) : sms;
+}
+
+bool decode_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int sms, DecodeWorkspace *w) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      num_q_heads % num_kv_heads != 0)
+    return false;
+  const int64_t G = num_q_heads / num_kv_heads;
+  const int64_t slots = 2 * static_cast<int64_t>(decode_grid_ctas(sms)) * pkv::kDecodeMaxWarps;
+  w->cnt_bytes = sizeof(uint32_t) * static_cast<size_t>(num_seqs) * num_kv_heads;
+  w->ml_offset = align_up(w->cnt_bytes, 256);
+  w->o_offset = align_up(w->ml_offset + static_cast<size_t>(slots * G * 2) * sizeof(float), 256);
+  w->total = w->o_offset + static_cast<size_t>(slots * G * head_dim) * sizeof(float);
   return true;
 }
 
@@ -187,34 +198,20 @@ pkv_status pkv_kv_store(const void *k, const void *v, void *k_cache, void *v_cac
   return PKV_OK;
 }
 
-size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
-                                 int32_t max_context_len) {
+size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_context_len) {
+  (void)max_context_len;  // the layout depends on the grid, not on context length
+  int sms = 0;
+  if (current_sm_count(&sms) != PKV_OK) return 0;
   DecodeWorkspace w;
-  if (!decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_context_len, &w)) return 0;
+  if (!decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, sms, &w)) return 0;
   return w.total;
 }
 
-int32_t pkv_decode_num_splits(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                              int32_t head_dim, int32_t max_context_len) {
-  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
-      max_context_len <= 0)
-    return -1;
-  int sms = 0;
-  if (current_sm_count(&sms) != PKV_OK) return -1;
-  pkv::DecodeArgs a{};
-  a.num_seqs = num_seqs;
-  a.num_q_heads = num_q_heads;
-  a.num_kv_heads = num_kv_heads;
-  a.head_dim = head_dim;
-  a.max_context_len = max_context_len;
-  const int64_t kps = static_cast<int64_t>(pkv::decode_chunks_per_split(
-                          a, sms, g_decode_chunks_override.load(std::memory_order_relaxed))) *
-                      pkv::kDecodeChunk;
-  return static_cast<int32_t>((max_context_len + kps - 1) / kps);
-}
-
-void pkv_decode_set_chunks_per_split(int32_t chunks) {
-  g_decode_chunks_override.store(chunks < 0 ? 0 : chunks, std::memory_order_relaxed);
+void pkv_decode_set_config(int32_t ctas, int32_t variant) {
+  g_decode_ctas.store(ctas < 0 ? 0 : ctas, std::memory_order_relaxed);
+  g_decode_variant.store(variant < 0 || variant >= pkv::kDecodeNumVariants ? 0 : variant,
+                         std::memory_order_relaxed);
 }
 
 pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
@@ -231,23 +228,25 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
   pkv_status st = check_attention_shape(num_q_heads, num_kv_heads, head_dim, block_size,
                                         num_blocks, max_blocks_per_seq);
   if (st != PKV_OK) return st;
-  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs > pkv::kDecodeMaxSeqs) return PKV_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PKV_ERR_INVALID_ARG;
-  DecodeWorkspace w;
-  decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_context_len, &w);
-  if (workspace == nullptr || workspace_bytes < w.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace == nullptr) return PKV_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned16(workspace)) return PKV_ERR_INVALID_ARG;
-
   int sms = 0;
   if ((st = current_sm_count(&sms)) != PKV_OK) return st;
+  DecodeWorkspace w;
+  decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, sms, &w);
+  if (workspace_bytes < w.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
+
   pkv::DecodeArgs a;
   a.q = q;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
   a.out = out;
   a.lse = lse;
-  a.ws_lse = static_cast<float *>(workspace);
+  a.ws_cnt = static_cast<uint32_t *>(workspace);
+  a.ws_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.ml_offset);
   a.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.o_offset);
   a.max_blocks = max_blocks_per_seq;
   a.max_context_len = max_context_len;
@@ -257,20 +256,22 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
   a.head_dim = head_dim;
   a.block_size = block_size;
   a.num_blocks = static_cast<int32_t>(num_blocks);
+  a.grid = decode_grid_ctas(sms);
+  a.variant = g_decode_variant.load(std::memory_order_relaxed);
   a.scale_log2 = scale * kLog2e;
-  a.chunks_per_split = pkv::decode_chunks_per_split(
-      a, sms, g_decode_chunks_override.load(std::memory_order_relaxed));
-  const int64_t kps = static_cast<int64_t>(a.chunks_per_split) * pkv::kDecodeChunk;
-  a.num_splits = static_cast<int32_t>((max_context_len + kps - 1) / kps);
-  if (a.num_splits > 65535) return PKV_ERR_UNSUPPORTED;
 
-  CUtensorMap kmap, vmap;
+  CUtensorMap kmap, vmap, qmap;
   const int64_t rows = num_blocks * block_size;
-  if ((st = encode_rows_map(&kmap, k_cache, rows, num_kv_heads, head_dim, 128, 16, false)) != PKV_OK)
+  const uint32_t G = static_cast<uint32_t>(num_q_heads / num_kv_heads);
+  if ((st = encode_rows_map(&kmap, k_cache, rows, num_kv_heads, head_dim, 128, 1, 16, false)) !=
+      PKV_OK)
     return st;
-  if ((st = encode_rows_map(&vmap, v_cache, rows, num_kv_heads, head_dim, 128, 16, false)) != PKV_OK)
+  if ((st = encode_rows_map(&vmap, v_cache, rows, num_kv_heads, head_dim, 128, 1, 16, false)) !=
+      PKV_OK)
     return st;
-  cudaError_t e = pkv::launch_decode(a, kmap, vmap, static_cast<cudaStream_t>(stream));
+  if ((st = encode_rows_map(&qmap, q, num_seqs, num_q_heads, head_dim, 128, G, 1, false)) != PKV_OK)
+    return st;
+  cudaError_t e = pkv::launch_decode(a, kmap, vmap, qmap, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PKV_OK;
 }
@@ -328,11 +329,11 @@ pkv_status pkv_paged_prefill_attn(const void *q, const void *k_cache, const void
 
   CUtensorMap qmap, kmap, vmap;
   const int64_t rows = num_blocks * block_size;
-  if ((st = encode_rows_map(&qmap, q, total_q, num_q_heads, head_dim, 64, 128, true)) != PKV_OK)
+  if ((st = encode_rows_map(&qmap, q, total_q, num_q_heads, head_dim, 64, 1, 128, true)) != PKV_OK)
     return st;
-  if ((st = encode_rows_map(&kmap, k_cache, rows, num_kv_heads, head_dim, 64, 16, true)) != PKV_OK)
+  if ((st = encode_rows_map(&kmap, k_cache, rows, num_kv_heads, head_dim, 64, 1, 16, true)) != PKV_OK)
     return st;
-  if ((st = encode_rows_map(&vmap, v_cache, rows, num_kv_heads, head_dim, 64, 16, true)) != PKV_OK)
+  if ((st = encode_rows_map(&vmap, v_cache, rows, num_kv_heads, head_dim, 64, 1, 16, true)) != PKV_OK)
     return st;
   cudaError_t e = pkv::launch_prefill(a, qmap, kmap, vmap, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");

@@ -48,14 +48,15 @@ extern "C" pkv_status pkv_paged_decode_attn_noalloc(
     int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t max_context_len,
     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
     int32_t block_size, int64_t num_blocks, float scale, void *out, float *lse, void *stream) {
-  const size_t need = pkv_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len);
+  const size_t need =
+      pkv_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len);
   if (need == 0) return PKV_ERR_INVALID_ARG;
   if (need > kScratchBytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
   void *scratch = nullptr;
   const pkv_status st = scratch_for_current_device(&scratch);
   if (st != PKV_OK) return st;
-  // Nothing in the scratch has to start at zero: each call writes every partial
-  // result it reads back.
+  // The only part of the scratch that must start at zero, the arrival
+  // counters, is cleared on the stream by the decode call itself.
   return pkv_paged_decode_attn(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                                max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
                                block_size, num_blocks, scale, out, lse, scratch, kScratchBytes,

@@ -23,7 +23,16 @@ cudaError_t take_kv_store_errors(cudaStream_t stream, uint32_t *flags);
 
 // ---------------------------------------------------------------- decode
 constexpr int kDecodeChunk = 32;          // keys per chunk (one TMA round per warp)
-constexpr int kDecodeMinChunksPerSplit = 2;
+constexpr int kDecodeMaxSeqs = 2048;      // sequences per call (chunk prefix lives in smem)
+
+// Launch shapes of the persistent decode kernel: warps per CTA and TMA stages
+// per warp. Variant 0 is the default.
+struct DecodeVariant {
+  int warps, stages;
+};
+constexpr DecodeVariant kDecodeVariants[] = {{6, 2}, {4, 3}, {12, 1}, {8, 1}};
+constexpr int kDecodeNumVariants = 4;
+constexpr int kDecodeMaxWarps = 12;
 
 struct DecodeArgs {
   const void *q;
@@ -31,20 +40,20 @@ struct DecodeArgs {
   const int32_t *context_lens;
   void *out;
   float *lse;
-  float *ws_o;            // [S, H_q, J, D] per-split normalised partial outputs
-  float *ws_lse;          // [S, H_q, J] per-split log2-sum-exp
+  float *ws_o;            // [2W, G, D] partial outputs of pairs cut by warp ranges
+  float *ws_ml;           // [2W, G, 2] their (max, sum), base 2
+  uint32_t *ws_cnt;       // [S * H_kv] arrival counters (zeroed before the kernel)
   int32_t max_blocks;
   int32_t max_context_len;
   int32_t num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
   int32_t num_blocks;
-  int32_t chunks_per_split; // keys per split = chunks_per_split * kDecodeChunk
-  int32_t num_splits;       // J = ceil(max_context_len / keys per split)
+  int32_t grid;             // CTAs (persistent; one per SM by default)
+  int32_t variant;          // index into kDecodeVariants
   float scale_log2;         // scale * log2(e)
 };
-// Plan: how many chunks per split for these sizes on a GPU with num_sms SMs.
-int32_t decode_chunks_per_split(const DecodeArgs &a, int num_sms, int32_t override_chunks);
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
-                          const CUtensorMap &v_map, cudaStream_t stream);
+                          const CUtensorMap &v_map, const CUtensorMap &q_map,
+                          cudaStream_t stream);
 cudaError_t take_decode_errors(cudaStream_t stream, uint32_t *flags);
 
 // ---------------------------------------------------------------- prefill

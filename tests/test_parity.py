@@ -21,9 +21,9 @@ SMALL = {c.name: c for c in W.all_small_cases()}
 
 @pytest.fixture(autouse=True)
 def _reset_knobs():
-    pkv.decode_set_chunks_per_split(0)
+    pkv.decode_set_config(0, 0)
     yield
-    pkv.decode_set_chunks_per_split(0)
+    pkv.decode_set_config(0, 0)
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
@@ -88,14 +88,36 @@ def test_sweep64_layer_full():
     assert_close(got["out"], got["lse"], ref["out"], ref["lse"], "sweep64 layer 0")
 
 
-@pytest.mark.parametrize("chunks", [2, 3, 5, 8, 1024])
-def test_split_count_does_not_change_results(chunks):
+@pytest.mark.parametrize("ctas,variant", [(1, 0), (2, 0), (7, 0), (1000, 0), (0, 1), (0, 2),
+                                          (0, 3), (3, 2)])
+def test_decode_launch_shape_does_not_change_results(ctas, variant):
+    # the grid decides how pairs are cut between warps (1 CTA: whole pairs per
+    # warp; 1000 CTAs: more warps than chunks); the variant decides warps/stages
+    for case in (SMALL["ragged256/decode"], SMALL["tiny/decode"]):
+        ref = oracle_run(case)
+        pkv.decode_set_config(ctas, variant)
+        got = gpu_run(case)
+        assert got["flags"] == 0
+        assert_close(got["out"], got["lse"], ref["out"], ref["lse"], f"{case.name} {ctas}/{variant}")
+
+
+def test_decode_repeated_calls_reuse_the_workspace():
     case = SMALL["ragged256/decode"]
     ref = oracle_run(case)
-    pkv.decode_set_chunks_per_split(chunks)
-    got = gpu_run(case)
-    assert got["flags"] == 0
-    assert_close(got["out"], got["lse"], ref["out"], ref["lse"], f"chunks={chunks}")
+    kc, vc = gpu_pool(case)
+    gpu_store(case.history, kc, vc)
+    gpu_store(case.step.new, kc, vc)
+    st = case.step
+    q, bt, ctx = dev_bf16(st.q), dev_i32(case.block_tables), dev_i32(st.context_lens)
+    ws = torch.empty(pkv.decode_workspace_size(case.num_seqs, case.H_q, case.H_kv, case.D,
+                                               st.max_context_len), dtype=torch.uint8,
+                     device="cuda")
+    for _ in range(3):
+        out, lse = pkv.paged_decode_attn(q, kc, vc, bt, ctx, st.max_context_len, case.scale,
+                                         workspace=ws)
+        assert_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref["out"],
+                     ref["lse"], "repeat")
+    assert pkv.check_device_errors() == 0
 
 
 @pytest.mark.parametrize("kind", ["decode", "prefill"])

@@ -35,7 +35,7 @@ def _noalloc(L, case, q, kc, vc, bt, ctx, out, lse):
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
     pkv_build.build()
     L = pkv.lib()
-    pkv.decode_set_chunks_per_split(0)
+    pkv.decode_set_config(0, 0)
     # two calls in a row with different sizes: the second reuses the scratch
     for case in (W.ragged256_decode(), W.tiny_decode()):
         kc, vc = gpu_pool(case)
@@ -63,13 +63,13 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     q, bt, ctx = dev_bf16(case.step.q), dev_i32(case.block_tables), dev_i32(case.step.context_lens)
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
-    P = ctypes.c_void_p
-    big_ctx = 1 << 20  # a million-token bound needs far more than the static scratch
-    assert pkv.decode_workspace_size(q.shape[0], case.H_q, case.D, big_ctx) > \
-        pkv.DECODE_NOALLOC_SCRATCH_BYTES
-    rc = L.pkv_paged_decode_attn_noalloc(
-        P(q.data_ptr()), P(kc.data_ptr()), P(vc.data_ptr()), P(bt.data_ptr()), bt.shape[1],
-        P(ctx.data_ptr()), big_ctx, q.shape[0], case.H_q, case.H_kv, case.D, case.block_size,
-        case.num_blocks, ctypes.c_float(case.scale), P(out.data_ptr()), P(lse.data_ptr()),
-        P(torch.cuda.current_stream().cuda_stream))
+    # a 4000-CTA grid needs more partial-result slots than the static scratch holds
+    pkv.decode_set_config(4000, 0)
+    try:
+        assert pkv.decode_workspace_size(q.shape[0], case.H_q, case.H_kv, case.D,
+                                         case.step.max_context_len) > \
+            pkv.DECODE_NOALLOC_SCRATCH_BYTES
+        rc = _noalloc(L, case, q, kc, vc, bt, ctx, out, lse)
+    finally:
+        pkv.decode_set_config(0, 0)
     assert rc == pkv.PKV_ERR_WORKSPACE_TOO_SMALL
