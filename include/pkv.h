@@ -130,7 +130,7 @@ size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t 
  *   out            device bf16 [num_seqs, num_q_heads, head_dim]
  *   lse            device float32 [num_seqs, num_q_heads], or NULL
  *   workspace      device, >= pkv_decode_workspace_size(...) bytes, 16-byte aligned
- * num_seqs is at most 2048.
+ * num_seqs is at most 1024.
  * Rows whose context_len is invalid raise PKV_DEVERR_CONTEXT and are not written.
  */
 pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
@@ -144,8 +144,8 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
 /*
  * Tuning knob of the decode launch, process-wide (not thread-safe against
  * concurrent launches): ctas = number of persistent CTAs (0 = one per SM, the
- * default); variant = launch shape (0 = default; 1..3 trade warps per CTA for
- * TMA stages per warp). Results do not depend on either, beyond rounding.
+ * default); variant = launch shape (0 = default, three TMA stages per CTA;
+ * 1 = two stages). Results do not depend on either, beyond rounding.
  * A non-default ctas changes pkv_decode_workspace_size.
  */
 void pkv_decode_set_config(int32_t ctas, int32_t variant);

@@ -139,7 +139,7 @@ def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_con
                                                max_context_len))
 
 
-DECODE_NUM_VARIANTS = 4
+DECODE_NUM_VARIANTS = 2
 
 
 def decode_set_config(ctas: int = 0, variant: int = 0) -> None:

@@ -9,7 +9,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/pkv.h"
+#include "pkv.h"
 #include "internal.h"
 
 namespace {
@@ -128,9 +128,8 @@ pkv_status check_attention_shape(int32_t num_q_heads, int32_t num_kv_heads, int3
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Decode workspace layout: arrival counters [S * H_kv], then per-warp partial
-// (max, sum) [2W, G, 2] and partial outputs [2W, G, D], for W = grid warps of
-// the widest launch variant.
+// Decode workspace layout: arrival counters [S * H_kv], then per-CTA partial
+// (max, sum) [2 grid, HG, G, 2] and partial outputs [2 grid, HG, G, D].
 struct DecodeWorkspace {
   size_t cnt_bytes, ml_offset, o_offset, total;
 };
@@ -145,12 +144,13 @@ bool decode_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       num_q_heads % num_kv_heads != 0)
     return false;
-  const int64_t G = num_q_heads / num_kv_heads;
-  const int64_t slots = 2 * static_cast<int64_t>(decode_grid_ctas(sms)) * pkv::kDecodeMaxWarps;
+  const int64_t heads = static_cast<int64_t>(pkv::decode_group_heads(num_kv_heads)) *
+                        (num_q_heads / num_kv_heads);
+  const int64_t slots = 2 * static_cast<int64_t>(decode_grid_ctas(sms));
   w->cnt_bytes = sizeof(uint32_t) * static_cast<size_t>(num_seqs) * num_kv_heads;
   w->ml_offset = align_up(w->cnt_bytes, 256);
-  w->o_offset = align_up(w->ml_offset + static_cast<size_t>(slots * G * 2) * sizeof(float), 256);
-  w->total = w->o_offset + static_cast<size_t>(slots * G * head_dim) * sizeof(float);
+  w->o_offset = align_up(w->ml_offset + static_cast<size_t>(slots * heads * 2) * sizeof(float), 256);
+  w->total = w->o_offset + static_cast<size_t>(slots * heads * head_dim) * sizeof(float);
   return true;
 }
 
@@ -260,16 +260,19 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
   a.variant = g_decode_variant.load(std::memory_order_relaxed);
   a.scale_log2 = scale * kLog2e;
 
+  // one box = 16 token rows of a head group (K, V), or the group's q rows
   CUtensorMap kmap, vmap, qmap;
   const int64_t rows = num_blocks * block_size;
   const uint32_t G = static_cast<uint32_t>(num_q_heads / num_kv_heads);
-  if ((st = encode_rows_map(&kmap, k_cache, rows, num_kv_heads, head_dim, 128, 1, 16, false)) !=
-      PKV_OK)
+  const uint32_t HG = static_cast<uint32_t>(pkv::decode_group_heads(num_kv_heads));
+  if ((st = encode_rows_map(&kmap, k_cache, rows, num_kv_heads, head_dim, 128, HG,
+                            pkv::kDecodeChunk, false)) != PKV_OK)
     return st;
-  if ((st = encode_rows_map(&vmap, v_cache, rows, num_kv_heads, head_dim, 128, 1, 16, false)) !=
-      PKV_OK)
+  if ((st = encode_rows_map(&vmap, v_cache, rows, num_kv_heads, head_dim, 128, HG,
+                            pkv::kDecodeChunk, false)) != PKV_OK)
     return st;
-  if ((st = encode_rows_map(&qmap, q, num_seqs, num_q_heads, head_dim, 128, G, 1, false)) != PKV_OK)
+  if ((st = encode_rows_map(&qmap, q, num_seqs, num_q_heads, head_dim, 128, HG * G, 1, false)) !=
+      PKV_OK)
     return st;
   cudaError_t e = pkv::launch_decode(a, kmap, vmap, qmap, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");

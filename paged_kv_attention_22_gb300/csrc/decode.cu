@@ -5,31 +5,30 @@
 //
 // One persistent kernel on CUDA cores, bound by HBM bandwidth:
 //
-//   Work list. The keys of every (sequence s, KV head g) pair are cut into
-//   32-key chunks; pairs are listed in (s, g) order, so the whole call is one
-//   list of C chunks. The grid holds one CTA per SM with NW warps, and the list
-//   is cut into W = min(grid * NW, C) equal contiguous ranges, one per warp:
-//   every warp moves the same number of bytes whatever the mix of context
-//   lengths, and no wave of CTAs is left half full.
+//   Work list. A unit is 16 consecutive keys of one sequence for a group of
+//   HG KV heads (all 8 heads of a Qwen3-0.6B layer): in the cache layout
+//   [block, slot, head, dim] those keys are 16 contiguous token rows, so one
+//   TMA box moves the whole unit's K (32 KiB for 8 heads) and one its V. Units
+//   are listed in (sequence, head group, chunk) order and the list is cut into
+//   min(grid, units) equal contiguous ranges, one per CTA (one CTA per SM):
+//   every SM moves the same number of bytes whatever the mix of context
+//   lengths, in large contiguous copies.
 //
-//   Streaming. Each warp runs its own NS-deep ring of shared-memory stages:
-//   lane 0 issues, per chunk, two 16-row TMA boxes of K and two of V (a box
-//   never crosses a cache block since block_size is a multiple of 16) and,
-//   for the first chunk of a segment, the pair's G query rows; the warp
-//   computes one chunk while the next ones land.
+//   Warps. One producer warp streams the CTA's units through an NS-deep ring of
+//   shared-memory stages (K box, V box and, when a unit opens a segment, the q
+//   rows of the group), each stage freed when all consumer warps are done with
+//   it. Consumer warp g owns KV head g of the group and its G query heads:
+//   logits with one 8-lane group per key and a transposing butterfly (each
+//   lane ends with one key's logit), online softmax in base 2, then P.V with
+//   half-warps on alternate keys.
 //
-//   Math. Logits with one 8-lane group per key and a transposing butterfly
-//   reduction (each lane ends with one key's logit), chunk-wise online softmax
-//   in base 2, then P.V with half-warps on alternate keys; the G query heads
-//   of a KV head share every staged byte.
-//
-//   Merge. A pair that lies inside one warp's range is finished by that warp.
-//   A pair cut by range boundaries leaves one (max, sum, output) partial per
-//   warp in the workspace: the first segment of warp w goes to slot 2w, its
-//   last segment (if different) to slot 2w+1. Each such warp then bumps the
-//   pair's arrival counter, and the last one to arrive merges the partials and
-//   writes the row. Nothing waits on another CTA. The counters are zeroed on
-//   the stream right before the kernel.
+//   Merge. A (sequence, KV head) whose keys all fall in one CTA's range is
+//   finished by that CTA's warp. One cut by range boundaries leaves one
+//   (max, sum, output) partial per CTA in the workspace: a CTA's first segment
+//   goes to slot 2c, its last segment (if different) to slot 2c+1. Each such
+//   warp then bumps the pair's arrival counter, and the last to arrive merges
+//   the partials and writes the row. Nothing waits on another CTA. The counters
+//   are zeroed on the stream right before the kernel.
 //
 // The 2-wide GQA group makes the logits and P.V skinny matrix-vector products,
 // so the kernel is bound by HBM bandwidth, not by any tensor-core contraction.
@@ -43,11 +42,9 @@ static __device__ uint32_t g_decode_errors;
 namespace {
 
 constexpr int kD = 128;                 // head dim (the only one supported)
-constexpr int kChunk = kDecodeChunk;    // 32 keys
-constexpr int kBoxRows = 16;            // rows per TMA box
+constexpr int kChunk = kDecodeChunk;    // 16 keys per unit
 constexpr int kRowBytes = kD * 2;       // 256 bytes of one head's K (or V) row
-constexpr int kBoxBytes = kBoxRows * kRowBytes;          // 4 KiB
-constexpr int kKVBytes = 2 * kChunk * kRowBytes;         // K + V of a chunk: 16 KiB
+constexpr int kMaxHG = kDecodeMaxGroupHeads;
 constexpr float kLn2 = 0.693147180559945309f;
 
 struct DecodeParams {
@@ -60,100 +57,67 @@ struct DecodeParams {
   uint32_t *ws_cnt;
   int32_t max_blocks, max_context_len, num_seqs, num_q_heads, num_kv_heads, block_size,
       num_blocks;
+  int32_t hg;        // KV heads per group (= consumer warps)
+  int32_t n_groups;  // num_kv_heads / hg
   float scale_log2;
 };
 
-template <int G, int NW, int NS>
+// Shared memory layout for G query heads per KV head and NS stages, sized for
+// the largest head group.
+template <int G, int NS>
 struct DecodeSmem {
-  static constexpr int kQBytes = G * kRowBytes;
-  static constexpr int kStageBytes = kKVBytes + kQBytes;        // K, V, then the q rows
-  static constexpr int kStagesBytes = NW * NS * kStageBytes;
-  static constexpr int kProbOffset = kStagesBytes;              // float [NW][G][32]
-  static constexpr int kProbBytes = NW * kChunk * G * 4;
-  static constexpr int kBarOffset = kProbOffset + kProbBytes;   // u64 [NW][NS]
-  static constexpr int kBarBytes = NW * NS * 8;
-  static constexpr int kPrefixOffset = kBarOffset + kBarBytes;  // int [S + 1] chunk prefix
+  static constexpr int kKBytes = kChunk * kMaxHG * kRowBytes;     // 32 KiB
+  static constexpr int kQBytes = kMaxHG * G * kRowBytes;
+  static constexpr int kStageBytes = 2 * kKBytes + kQBytes;       // K, V, q rows
+  static constexpr int kProbOffset = NS * kStageBytes;            // float [HG][G][16]
+  static constexpr int kProbBytes = kMaxHG * G * kChunk * 4;
+  static constexpr int kBarOffset = kProbOffset + kProbBytes;     // u64 full[NS], empty[NS]
+  static constexpr int kPrefixOffset = kBarOffset + 2 * NS * 8;   // int [S + 1] chunk prefix
   static constexpr int total(int num_seqs) { return kPrefixOffset + 4 * (num_seqs + 1) + 128; }
 };
 
-// Position in the chunk list: sequence, KV head, chunk within the pair.
+// Position in the unit list: sequence, head group, chunk within the pair.
 struct Cursor {
-  int s, g, k;
+  int s, hg, k;
 };
 
 __device__ __forceinline__ int chunks_of(const int *prefix, int s) {
   return prefix[s + 1] - prefix[s];
 }
 
-// Cursor of global chunk c (c < C): sequence s owns H_kv * chunks_of(s)
-// consecutive chunks starting at H_kv * prefix[s].
-__device__ __forceinline__ Cursor locate(const int *prefix, int num_seqs, int H_kv, int64_t c) {
-  int lo = 0, hi = num_seqs - 1;  // largest s with H_kv * prefix[s] <= c (never empty)
+// Cursor of unit u (u < U): sequence s owns n_groups * chunks_of(s)
+// consecutive units starting at n_groups * prefix[s].
+__device__ __forceinline__ Cursor locate(const int *prefix, int num_seqs, int n_groups,
+                                         int64_t u) {
+  int lo = 0, hi = num_seqs - 1;  // largest s with n_groups * prefix[s] <= u (never empty)
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (static_cast<int64_t>(H_kv) * prefix[mid] <= c) lo = mid; else hi = mid - 1;
+    if (static_cast<int64_t>(n_groups) * prefix[mid] <= u) lo = mid; else hi = mid - 1;
   }
   const int n = chunks_of(prefix, lo);
-  const int64_t r = c - static_cast<int64_t>(H_kv) * prefix[lo];
+  const int64_t r = u - static_cast<int64_t>(n_groups) * prefix[lo];
   return Cursor{lo, static_cast<int>(r / n), static_cast<int>(r % n)};
 }
 
-// Next chunk in list order; past the last chunk, s becomes num_seqs.
-__device__ __forceinline__ void advance(Cursor &cur, const int *prefix, int num_seqs, int H_kv) {
+// Next unit in list order; past the last unit, s becomes num_seqs.
+__device__ __forceinline__ void advance(Cursor &cur, const int *prefix, int num_seqs,
+                                        int n_groups) {
   if (++cur.k < chunks_of(prefix, cur.s)) return;
   cur.k = 0;
-  if (++cur.g < H_kv) return;
-  cur.g = 0;
+  if (++cur.hg < n_groups) return;
+  cur.hg = 0;
   do {
     ++cur.s;
   } while (cur.s < num_seqs && chunks_of(prefix, cur.s) == 0);
 }
 
-// First chunk of warp w's range among W warps over C chunks (W <= C, so every
-// range is non-empty), and the warp whose range holds chunk c.
-__device__ __forceinline__ int64_t range_start(int64_t w, int64_t W, int64_t C) {
-  return w * C / W;
+// First unit of CTA c's range among W CTAs over U units (W <= U, so every range
+// is non-empty), and the CTA whose range holds unit u.
+__device__ __forceinline__ int64_t range_start(int64_t c, int64_t W, int64_t U) {
+  return c * U / W;
 }
-__device__ __forceinline__ int64_t owner_of(int64_t c, int64_t W, int64_t C) {
-  return ((c + 1) * W + C - 1) / C - 1;
-}
-
-// Issue chunk `cur` into a stage: K and V boxes, plus the q rows when it opens
-// a segment. The stage's barrier completes when every issued byte has landed.
-template <int G>
-__device__ __forceinline__ void issue_chunk(const CUtensorMap *k_map, const CUtensorMap *v_map,
-                                            const CUtensorMap *q_map, const DecodeParams &p,
-                                            const Cursor &cur, bool with_q, uint32_t stage,
-                                            uint32_t bar, uint64_t policy) {
-  const int ctx = p.context_lens[cur.s];
-  const int key0 = cur.k * kChunk;
-  int32_t rows[2];
-  uint32_t bytes = with_q ? G * kRowBytes : 0;
-#pragma unroll
-  for (int b = 0; b < 2; ++b) {
-    rows[b] = -1;
-    const int kb = key0 + b * kBoxRows;
-    if (kb < ctx) {
-      const int32_t blk =
-          p.block_tables[static_cast<int64_t>(cur.s) * p.max_blocks + kb / p.block_size];
-      if (blk < 0 || blk >= p.num_blocks) {
-        atomicOr(&g_decode_errors, kErrBlock);
-      } else {
-        rows[b] = blk * p.block_size + kb % p.block_size;
-        bytes += 2 * kBoxBytes;
-      }
-    }
-  }
-  mbar_arrive_expect_tx(bar, bytes);
-#pragma unroll
-  for (int b = 0; b < 2; ++b) {
-    if (rows[b] >= 0) {
-      tma_load_3d_hint(stage + b * kBoxBytes, k_map, bar, 0, cur.g, rows[b], policy);
-      tma_load_3d_hint(stage + kChunk * kRowBytes + b * kBoxBytes, v_map, bar, 0, cur.g, rows[b],
-                       policy);
-    }
-  }
-  if (with_q) tma_load_3d(stage + kKVBytes, q_map, bar, 0, cur.g * G, cur.s);
+__device__ __forceinline__ int64_t owner_of(int64_t u, int64_t W, int64_t U) {
+  return ((u + 1) * W + U - 1) / U - 1;
 }
 
 // One step of the transposing butterfly: lanes whose sub-index bit is set keep
@@ -169,18 +133,19 @@ __device__ __forceinline__ void butterfly_half(float (&x)[N], bool upper, int la
   }
 }
 
-template <int G, int NW, int NS>
-__global__ void __launch_bounds__(NW * 32, 1)
+template <int G, int NS>
+__global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap k_map,
                   const __grid_constant__ CUtensorMap v_map,
                   const __grid_constant__ CUtensorMap q_map, const DecodeParams p) {
-  using L = DecodeSmem<G, NW, NS>;
+  using L = DecodeSmem<G, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                               ~static_cast<uintptr_t>(127));
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int H_kv = p.num_kv_heads;
+  const int HG = p.hg;
+  const int n_groups = p.n_groups;
 
   // a CTA gave up waiting (in this or an earlier launch): skip the work until
   // the error word is read and cleared; decided once per CTA
@@ -190,6 +155,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
   // ---- chunk prefix over sequences (invalid lengths count as empty)
   int *prefix = reinterpret_cast<int *>(smem + L::kPrefixOffset);
+  const uint32_t full0 = smem_u32(smem + L::kBarOffset);
+  const uint32_t empty0 = full0 + NS * 8;
   if (warp == 0) {
     int carry = 0;
     const int64_t ctx_cap = static_cast<int64_t>(p.max_blocks) * p.block_size;
@@ -213,70 +180,93 @@ __global__ void __launch_bounds__(NW * 32, 1)
       if (s < p.num_seqs) prefix[s] = carry + incl - n;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) prefix[p.num_seqs] = carry;
+    if (lane == 0) {
+      prefix[p.num_seqs] = carry;
+      for (int i = 0; i < NS; ++i) {
+        mbar_init(full0 + 8 * i, 1);
+        mbar_init(empty0 + 8 * i, HG);
+      }
+      fence_barrier_init();
+    }
   }
   __syncthreads();
 
-  const int64_t C = static_cast<int64_t>(H_kv) * prefix[p.num_seqs];
-  const int64_t W_all = static_cast<int64_t>(gridDim.x) * NW;
-  const int64_t W = W_all < C ? W_all : C;
-  const int64_t w = static_cast<int64_t>(blockIdx.x) * NW + warp;
-  if (w >= W) return;  // no chunks for this warp (no CTA-wide sync follows)
-  const int64_t c_lo = range_start(w, W, C), c_hi = range_start(w + 1, W, C);
-  const int n_mine = static_cast<int>(c_hi - c_lo);
+  const int64_t U = static_cast<int64_t>(n_groups) * prefix[p.num_seqs];
+  const int64_t W = static_cast<int64_t>(gridDim.x) < U ? static_cast<int64_t>(gridDim.x) : U;
+  const int64_t cta = blockIdx.x;
+  if (cta >= W) return;  // no units for this CTA
+  const int64_t u_lo = range_start(cta, W, U), u_hi = range_start(cta + 1, W, U);
+  const int n_mine = static_cast<int>(u_hi - u_lo);
+  const uint32_t stage0 = smem_u32(smem);
 
-  const uint32_t stage0 = smem_u32(smem) + static_cast<uint32_t>(warp * NS) * L::kStageBytes;
-  const uint32_t bar0 = smem_u32(smem + L::kBarOffset) + warp * NS * 8;
-  float *prob = reinterpret_cast<float *>(smem + L::kProbOffset) + warp * kChunk * G;
-  const uint64_t policy = l2_policy_evict_first();
-
-  // the issue cursor runs up to NS chunks ahead of the compute cursor
-  Cursor icur = locate(prefix, p.num_seqs, H_kv, c_lo);
-  Cursor ccur = icur;
-  if (lane == 0) {
-    if (warp == 0) {
+  if (warp == HG) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
       prefetch_tensormap(&k_map);
       prefetch_tensormap(&v_map);
       prefetch_tensormap(&q_map);
+      const uint64_t policy = l2_policy_evict_first();
+      Cursor cur = locate(prefix, p.num_seqs, n_groups, u_lo);
+      const uint32_t box = static_cast<uint32_t>(kChunk * HG * kRowBytes);
+      const uint32_t qbox = static_cast<uint32_t>(HG * G * kRowBytes);
+      for (int i = 0; i < n_mine; ++i) {
+        const int st = i % NS;
+        if (i >= NS && !mbar_wait(empty0 + 8 * st, ((i / NS) - 1) & 1, &g_decode_errors)) {
+          atomicOr(&g_decode_errors, kErrTimeout);
+          break;
+        }
+        const uint32_t stage = stage0 + st * L::kStageBytes;
+        const uint32_t bar = full0 + 8 * st;
+        const bool with_q = (i == 0) || (cur.k == 0);
+        const int key0 = cur.k * kChunk;
+        const int32_t blk =
+            p.block_tables[static_cast<int64_t>(cur.s) * p.max_blocks + key0 / p.block_size];
+        const bool ok = blk >= 0 && blk < p.num_blocks;
+        if (!ok) atomicOr(&g_decode_errors, kErrBlock);
+        mbar_arrive_expect_tx(bar, (ok ? 2 * box : 0) + (with_q ? qbox : 0));
+        if (ok) {
+          const int32_t row = blk * p.block_size + key0 % p.block_size;
+          tma_load_3d_hint(stage, &k_map, bar, 0, cur.hg * HG, row, policy);
+          tma_load_3d_hint(stage + L::kKBytes, &v_map, bar, 0, cur.hg * HG, row, policy);
+        }
+        if (with_q) tma_load_3d(stage + 2 * L::kKBytes, &q_map, bar, 0, cur.hg * HG * G, cur.s);
+        advance(cur, prefix, p.num_seqs, n_groups);
+      }
     }
-#pragma unroll
-    for (int i = 0; i < NS; ++i) mbar_init(bar0 + 8 * i, 1);
-    fence_barrier_init();
+    return;
   }
-  __syncwarp();
-  for (int i = 0; i < NS && i < n_mine; ++i) {
-    if (lane == 0)
-      issue_chunk<G>(&k_map, &v_map, &q_map, p, icur, i == 0 || icur.k == 0,
-                     stage0 + i * L::kStageBytes, bar0 + 8 * i, policy);
-    advance(icur, prefix, p.num_seqs, H_kv);
-  }
+  if (warp > HG) return;
 
+  // -------------------------------------------------------------- consumers
+  const int g = warp;                      // KV head within the group
+  const int tok_bytes = HG * kRowBytes;    // one token row of the group in a stage
   const int sub = lane & 7, grp = lane >> 3;
-  const int my_key = 4 * sub + grp;        // key owned after the butterfly
+  const int my_key = 4 * (sub >> 1) + grp; // key whose logit this lane holds
+  const bool counts = (sub & 1) == 0;      // lanes sub, sub^1 hold the same key
   const int half = lane >> 4, vcol = lane & 15;
+  float *prob = reinterpret_cast<float *>(smem + L::kProbOffset) + g * G * kChunk;
+  Cursor cur = locate(prefix, p.num_seqs, n_groups, u_lo);
   float qf[G][16];
   float m[G], lsum[G], o[G][8];
-  int seg_first_k = 0;                     // chunk index (in the pair) opening the segment
-  bool seg_is_first = true;                // segment opened at this warp's range start
+  int seg_first_k = 0;
+  bool seg_is_first = true;
   int ctx = 0;
 
 #pragma unroll 1
   for (int it = 0; it < n_mine; ++it) {
     const int st = it % NS;
-    const uint32_t stage = stage0 + st * L::kStageBytes;
-    const uint8_t *kst = smem + static_cast<size_t>(warp * NS + st) * L::kStageBytes;
-    const uint8_t *vst = kst + kChunk * kRowBytes;
-    const bool opens = (it == 0) || (ccur.k == 0);
-    if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * st, (it / NS) & 1, &g_decode_errors))) {
+    const uint8_t *kst = smem + static_cast<size_t>(st) * L::kStageBytes;
+    const uint8_t *vst = kst + L::kKBytes;
+    const bool opens = (it == 0) || (cur.k == 0);
+    if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * st, (it / NS) & 1, &g_decode_errors))) {
       if (lane == 0) atomicOr(&g_decode_errors, kErrTimeout);
-      return;  // a lost copy: rows of this warp's range stay unwritten
+      return;  // a lost copy: rows of this CTA's range stay unwritten
     }
     if (opens) {
-      // a new segment: its q rows came with this chunk
-      ctx = p.context_lens[ccur.s];
-      seg_first_k = ccur.k;
+      ctx = p.context_lens[cur.s];
+      seg_first_k = cur.k;
       seg_is_first = (it == 0);
-      const uint8_t *qs = kst + kKVBytes;
+      const uint8_t *qs = kst + 2 * L::kKBytes + g * G * kRowBytes;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const uint4 a = *reinterpret_cast<const uint4 *>(qs + h * kRowBytes + sub * 16);
@@ -295,13 +285,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
         for (int i = 0; i < 8; ++i) o[h][i] = 0.f;
       }
     }
-    const int nvalid = min(kChunk, ctx - ccur.k * kChunk);
+    const int nvalid = min(kChunk, ctx - cur.k * kChunk);
 
     // ---- logits: pass pp covers keys 4*pp + grp; lane group grp, sub-dims sub
-    float part[G][8];
+    float part[G][4];
 #pragma unroll
-    for (int pp = 0; pp < 8; ++pp) {
-      const uint8_t *krow = kst + (4 * pp + grp) * kRowBytes;
+    for (int pp = 0; pp < 4; ++pp) {
+      const uint8_t *krow = kst + (4 * pp + grp) * tok_bytes + g * kRowBytes;
       const uint4 ka = *reinterpret_cast<const uint4 *>(krow + sub * 16);
       const uint4 kb = *reinterpret_cast<const uint4 *>(krow + 128 + sub * 16);
       const uint32_t wv[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
@@ -319,28 +309,27 @@ __global__ void __launch_bounds__(NW * 32, 1)
     float sc[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      butterfly_half<8>(part[h], (sub & 4) != 0, 4);
-      float q4[4] = {part[h][0], part[h][1], part[h][2], part[h][3]};
-      butterfly_half<4>(q4, (sub & 2) != 0, 2);
-      float q2[2] = {q4[0], q4[1]};
-      butterfly_half<2>(q2, (sub & 1) != 0, 1);
-      sc[h] = my_key < nvalid ? q2[0] : -INFINITY;
+      butterfly_half<4>(part[h], (sub & 4) != 0, 4);
+      float q2[2] = {part[h][0], part[h][1]};
+      butterfly_half<2>(q2, (sub & 2) != 0, 2);
+      const float full = q2[0] + __shfl_xor_sync(0xffffffffu, q2[0], 1);
+      sc[h] = my_key < nvalid ? full : -INFINITY;
     }
 
-    // ---- online softmax over the chunk (base 2)
+    // ---- online softmax over the unit (base 2)
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       float mx = sc[h];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
       const float m_new = fmaxf(m[h], mx);
-      const float alpha = fast_exp2(m[h] - m_new);  // 0 on a segment's first chunk
+      const float alpha = fast_exp2(m[h] - m_new);  // 0 on a segment's first unit
       const float pr = fast_exp2(sc[h] - m_new);    // 0 for masked keys
-      lsum[h] = lsum[h] * alpha + pr;
+      lsum[h] = lsum[h] * alpha + (counts ? pr : 0.f);
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[h][i] *= alpha;
       m[h] = m_new;
-      prob[h * kChunk + my_key] = pr;
+      if (counts) prob[h * kChunk + my_key] = pr;
     }
     __syncwarp();
 
@@ -350,7 +339,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
       const int key = 2 * pp + half;
       if (2 * pp >= nvalid) break;
       if (key < nvalid) {
-        const uint4 vv = *reinterpret_cast<const uint4 *>(vst + key * kRowBytes + vcol * 16);
+        const uint4 vv =
+            *reinterpret_cast<const uint4 *>(vst + key * tok_bytes + g * kRowBytes + vcol * 16);
         const uint32_t wv[4] = {vv.x, vv.y, vv.z, vv.w};
         float pr[G];
 #pragma unroll
@@ -366,19 +356,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
         }
       }
     }
-    // every lane is done with this stage (and with prob) before it is refilled
-    fence_proxy_async_smem();
+    // this warp is done with the stage (and with prob): release it
     __syncwarp();
-    if (it + NS < n_mine) {
-      if (lane == 0)
-        issue_chunk<G>(&k_map, &v_map, &q_map, p, icur, icur.k == 0, stage, bar0 + 8 * st,
-                       policy);
-      advance(icur, prefix, p.num_seqs, H_kv);
-    }
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
 
-    // ---- segment end: the pair's last chunk, or this warp's last chunk
-    const int nch = chunks_of(prefix, ccur.s);
-    const bool pair_ends = ccur.k == nch - 1;
+    // ---- segment end: the pair's last unit, or this CTA's last unit
+    const int nch = chunks_of(prefix, cur.s);
+    const bool pair_ends = cur.k == nch - 1;
     if (pair_ends || it == n_mine - 1) {
       float lt[G];
 #pragma unroll
@@ -389,9 +373,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) lt[h] += __shfl_xor_sync(0xffffffffu, lt[h], off);
       }
-      const int64_t row0 = static_cast<int64_t>(ccur.s) * p.num_q_heads + ccur.g * G;
+      const int kvh = cur.hg * HG + g;  // KV head
+      const int64_t row0 = static_cast<int64_t>(cur.s) * p.num_q_heads + kvh * G;
       if (seg_first_k == 0 && pair_ends) {
-        // the whole pair is in this segment: write the final row
+        // the whole pair is in this segment: write the final rows
         if (lane < 16) {
 #pragma unroll
           for (int h = 0; h < G; ++h) {
@@ -410,11 +395,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
         }
       } else {
         // a piece of a pair cut by range boundaries: publish the partial
-        const int64_t slot = 2 * w + (seg_is_first ? 0 : 1);
+        const int64_t slot = 2 * cta + (seg_is_first ? 0 : 1);
+        const int64_t base = (slot * HG + g) * G;  // partial index of head h: base + h
         if (lane < 16) {
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (slot * G + h) * kD + vcol * 8);
+            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (base + h) * kD + vcol * 8);
             __stcg(dst, make_float4(o[h][0], o[h][1], o[h][2], o[h][3]));
             __stcg(dst + 1, make_float4(o[h][4], o[h][5], o[h][6], o[h][7]));
           }
@@ -422,49 +408,47 @@ __global__ void __launch_bounds__(NW * 32, 1)
         if (lane == 0) {
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            __stcg(p.ws_ml + (slot * G + h) * 2, m[h]);
-            __stcg(p.ws_ml + (slot * G + h) * 2 + 1, lt[h]);
+            __stcg(p.ws_ml + (base + h) * 2, m[h]);
+            __stcg(p.ws_ml + (base + h) * 2 + 1, lt[h]);
           }
         }
         __threadfence();
         __syncwarp();
-        const int64_t pair = static_cast<int64_t>(ccur.s) * H_kv + ccur.g;
-        const int64_t P0 =
-            static_cast<int64_t>(H_kv) * prefix[ccur.s] + static_cast<int64_t>(ccur.g) * nch;
-        const int64_t wa = owner_of(P0, W, C), wb = owner_of(P0 + nch - 1, W, C);
+        const int64_t P0 = static_cast<int64_t>(n_groups) * prefix[cur.s] +
+                           static_cast<int64_t>(cur.hg) * nch;
+        const int64_t wa = owner_of(P0, W, U), wb = owner_of(P0 + nch - 1, W, U);
         uint32_t arrived = 0;
-        if (lane == 0) arrived = atomicAdd(p.ws_cnt + pair, 1u) + 1u;
+        if (lane == 0)
+          arrived = atomicAdd(p.ws_cnt + static_cast<int64_t>(cur.s) * p.num_kv_heads + kvh, 1u) + 1u;
         arrived = __shfl_sync(0xffffffffu, arrived, 0);
         if (arrived == static_cast<uint32_t>(wb - wa + 1)) {
-          // last piece in: merge the pair's partials. Warp wa holds it in its
-          // last slot unless its range starts at the pair's first chunk.
+          // last piece in: merge the pair's partials. CTA wa holds it in its
+          // last slot unless its range starts at the pair's first unit.
           __threadfence();
-          const int64_t wa_slot = 2 * wa + (range_start(wa, W, C) < P0 ? 1 : 0);
+          const int64_t wa_slot = 2 * wa + (range_start(wa, W, U) < P0 ? 1 : 0);
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            // max and sum over the pieces: lanes split the pieces, then reduce
             float M = -INFINITY;
             for (int64_t x = wa + lane; x <= wb; x += 32) {
               const int64_t sl = x == wa ? wa_slot : 2 * x;
-              M = fmaxf(M, __ldcg(p.ws_ml + (sl * G + h) * 2));
+              M = fmaxf(M, __ldcg(p.ws_ml + ((sl * HG + g) * G + h) * 2));
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
             float Lsum = 0.f;
             for (int64_t x = wa + lane; x <= wb; x += 32) {
               const int64_t sl = x == wa ? wa_slot : 2 * x;
-              Lsum += __ldcg(p.ws_ml + (sl * G + h) * 2 + 1) *
-                      fast_exp2(__ldcg(p.ws_ml + (sl * G + h) * 2) - M);
+              const int64_t idx = (sl * HG + g) * G + h;
+              Lsum += __ldcg(p.ws_ml + idx * 2 + 1) * fast_exp2(__ldcg(p.ws_ml + idx * 2) - M);
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
-            // output: each lane owns 4 dims
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             for (int64_t x = wa; x <= wb; ++x) {
               const int64_t sl = x == wa ? wa_slot : 2 * x;
-              const float f = fast_exp2(__ldcg(p.ws_ml + (sl * G + h) * 2) - M);
-              const float4 ov =
-                  __ldcg(reinterpret_cast<const float4 *>(p.ws_o + (sl * G + h) * kD) + lane);
+              const int64_t idx = (sl * HG + g) * G + h;
+              const float f = fast_exp2(__ldcg(p.ws_ml + idx * 2) - M);
+              const float4 ov = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + idx * kD) + lane);
               acc[0] = fmaf(ov.x, f, acc[0]);
               acc[1] = fmaf(ov.y, f, acc[1]);
               acc[2] = fmaf(ov.z, f, acc[2]);
@@ -480,41 +464,34 @@ __global__ void __launch_bounds__(NW * 32, 1)
         }
       }
     }
-    advance(ccur, prefix, p.num_seqs, H_kv);
+    advance(cur, prefix, p.num_seqs, n_groups);
   }
 }
 
-template <int G, int NW, int NS>
+template <int G, int NS>
 cudaError_t launch_variant(const DecodeArgs &a, const CUtensorMap &k_map,
                            const CUtensorMap &v_map, const CUtensorMap &q_map,
                            const DecodeParams &p, cudaStream_t stream) {
-  using L = DecodeSmem<G, NW, NS>;
+  using L = DecodeSmem<G, NS>;
   static_assert(L::total(kDecodeMaxSeqs) <= 227 * 1024, "decode shared memory");
-  auto kern = decode_kernel<G, NW, NS>;
+  auto kern = decode_kernel<G, NS>;
   const int smem = L::total(a.num_seqs);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(p.ws_cnt, 0,
                       sizeof(uint32_t) * static_cast<size_t>(a.num_seqs) * a.num_kv_heads, stream);
   if (e != cudaSuccess) return e;
-  kern<<<a.grid, NW * 32, smem, stream>>>(k_map, v_map, q_map, p);
+  kern<<<a.grid, (p.hg + 1) * 32, smem, stream>>>(k_map, v_map, q_map, p);
   return cudaGetLastError();
 }
 
 template <int G>
 cudaError_t launch_group(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
                          const CUtensorMap &q_map, const DecodeParams &p, cudaStream_t stream) {
-  static_assert(kDecodeNumVariants == 4, "variant table");
-  switch (a.variant) {
-    case 1: return launch_variant<G, kDecodeVariants[1].warps, kDecodeVariants[1].stages>(
-        a, k_map, v_map, q_map, p, stream);
-    case 2: return launch_variant<G, kDecodeVariants[2].warps, kDecodeVariants[2].stages>(
-        a, k_map, v_map, q_map, p, stream);
-    case 3: return launch_variant<G, kDecodeVariants[3].warps, kDecodeVariants[3].stages>(
-        a, k_map, v_map, q_map, p, stream);
-    default: return launch_variant<G, kDecodeVariants[0].warps, kDecodeVariants[0].stages>(
-        a, k_map, v_map, q_map, p, stream);
-  }
+  static_assert(kDecodeNumVariants == 2, "variant table");
+  if (a.variant == 1)
+    return launch_variant<G, kDecodeVariants[1].stages>(a, k_map, v_map, q_map, p, stream);
+  return launch_variant<G, kDecodeVariants[0].stages>(a, k_map, v_map, q_map, p, stream);
 }
 
 }  // namespace
@@ -537,6 +514,8 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
   p.num_kv_heads = a.num_kv_heads;
   p.block_size = a.block_size;
   p.num_blocks = a.num_blocks;
+  p.hg = decode_group_heads(a.num_kv_heads);
+  p.n_groups = a.num_kv_heads / p.hg;
   p.scale_log2 = a.scale_log2;
   switch (a.num_q_heads / a.num_kv_heads) {
     case 1: return launch_group<1>(a, k_map, v_map, q_map, p, stream);

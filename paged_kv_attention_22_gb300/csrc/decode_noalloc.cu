@@ -10,7 +10,7 @@
 // belongs to this file, so it calls no allocator at all.
 #include <mutex>
 
-#include "../../include/pkv.h"
+#include "pkv.h"
 #include "internal.h"
 
 namespace {

@@ -22,17 +22,24 @@ cudaError_t launch_kv_store(const KvStoreArgs &a, cudaStream_t stream);
 cudaError_t take_kv_store_errors(cudaStream_t stream, uint32_t *flags);
 
 // ---------------------------------------------------------------- decode
-constexpr int kDecodeChunk = 32;          // keys per chunk (one TMA round per warp)
-constexpr int kDecodeMaxSeqs = 2048;      // sequences per call (chunk prefix lives in smem)
+constexpr int kDecodeChunk = 16;          // keys per unit (one TMA box of all heads of a group)
+constexpr int kDecodeMaxSeqs = 1024;      // sequences per call (chunk prefix lives in smem)
+constexpr int kDecodeMaxGroupHeads = 8;   // KV heads per CTA head group
 
-// Launch shapes of the persistent decode kernel: warps per CTA and TMA stages
-// per warp. Variant 0 is the default.
+// Launch shapes of the persistent decode kernel: TMA stages per CTA.
+// Variant 0 is the default.
 struct DecodeVariant {
-  int warps, stages;
+  int stages;
 };
-constexpr DecodeVariant kDecodeVariants[] = {{6, 2}, {4, 3}, {12, 1}, {8, 1}};
-constexpr int kDecodeNumVariants = 4;
-constexpr int kDecodeMaxWarps = 12;
+constexpr DecodeVariant kDecodeVariants[] = {{3}, {2}};
+constexpr int kDecodeNumVariants = 2;
+
+// KV heads per CTA head group: the largest divisor of H_kv that is <= 8.
+inline int decode_group_heads(int num_kv_heads) {
+  for (int d = kDecodeMaxGroupHeads; d > 1; --d)
+    if (num_kv_heads % d == 0) return d;
+  return 1;
+}
 
 struct DecodeArgs {
   const void *q;
@@ -40,8 +47,8 @@ struct DecodeArgs {
   const int32_t *context_lens;
   void *out;
   float *lse;
-  float *ws_o;            // [2W, G, D] partial outputs of pairs cut by warp ranges
-  float *ws_ml;           // [2W, G, 2] their (max, sum), base 2
+  float *ws_o;            // [2 grid, HG, G, D] partial outputs of pieces cut by CTA ranges
+  float *ws_ml;           // [2 grid, HG, G, 2] their (max, sum), base 2
   uint32_t *ws_cnt;       // [S * H_kv] arrival counters (zeroed before the kernel)
   int32_t max_blocks;
   int32_t max_context_len;

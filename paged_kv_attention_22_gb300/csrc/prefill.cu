@@ -6,20 +6,29 @@
 // "How lunaryes/nano-vllm works", where the block manager hands out cached
 // blocks). Query i of a segment sees keys p <= Lk - Lq + i.
 //
-// One CTA per (128-query tile, query head, sequence); 6 warps:
-//   warp 4  TMA producer: the Q tile once, then K and V tiles of 128 keys as
-//           eight 16-row boxes each (a box never crosses a cache block), two
-//           stages deep, 128-byte swizzled.
-//   warp 5  MMA issuer: S = Q K^T into TMEM (128 lanes x 128 fp32 columns),
-//           then O += P V into a second TMEM region; completion is signalled
-//           through tcgen05.commit on mbarriers. Before the P.V of the tile
-//           that holds the segment's last key it zeroes the V rows past it,
-//           so that stale or poisoned rows never meet a zero probability.
-//   warps 0-3  one query row per thread (TMEM lane = row): read the S row,
-//           mask, online softmax in base 2, rescale the O row in TMEM when the
-//           running max moves, write P (bf16) to shared memory in the swizzled
-//           K-major layout the MMA reads, and finally normalise O and store
-//           the bf16 output and the natural-log lse.
+// One CTA owns two 128-row query tiles that share every K/V tile: with grouped
+// queries (H_q / H_kv >= 2) the two query heads of a head pair over the same
+// 128 rows; without grouping, two consecutive row tiles of one head. 10 warps:
+//   warp 0     TMA producer: both Q tiles once, then K and V tiles of 128 keys
+//              as eight 16-row boxes each (a box never crosses a cache block),
+//              two stages deep, 128-byte swizzled.
+//   warp 1     MMA issuer. TMEM holds S_t (128 fp32 columns) and O_t (128) for
+//              each tile t. Per KV tile j and query tile t: S_t = Q_t K_j^T
+//              (A and B from shared memory), then, once the softmax has
+//              written P_t (bf16) over the first 64 columns of S_t,
+//              O_t += P_t V_j with A read straight from TMEM. S_t(j+1) is
+//              issued after P.V(j), and MMAs run in issue order, so a
+//              completed S_t(j+1) also means O_t holds every tile up to j.
+//              The V rows past the segment's last key are zeroed before their
+//              first P.V, so stale or poisoned rows never meet a zero
+//              probability.
+//   warps 2-5  softmax of tile 0, warps 6-9 softmax of tile 1: one query row
+//              per thread (TMEM lane = row). Read the S row, mask, online
+//              softmax in base 2 (the O row in TMEM is rescaled only in tiles
+//              where some row's maximum grows), write P back into TMEM; at the
+//              end normalise O and store the bf16 output and the natural-log
+//              lse.
+// While one tile's softmax runs, the tensor pipe works on the other tile.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -30,27 +39,27 @@ static __device__ uint32_t g_prefill_errors;
 namespace {
 
 constexpr int kD = 128;
-constexpr int kBM = 128;                       // query rows per CTA
+constexpr int kBM = 128;                       // query rows per tile
 constexpr int kBN = 128;                       // keys per KV tile
+constexpr int kTiles = 2;                      // query tiles per CTA
 constexpr int kBoxRows = 16;                   // rows per K/V TMA box
 constexpr int kHalfBytes = 128 * 128;          // 128 rows x 64 bf16 (one swizzle column group)
 constexpr int kTileBytes = 2 * kHalfBytes;     // 128 rows x 128 bf16
 constexpr int kStages = 2;
 constexpr int kQOff = 0;
-constexpr int kKOff = kQOff + kTileBytes;
+constexpr int kKOff = kQOff + kTiles * kTileBytes;
 constexpr int kVOff = kKOff + kStages * kTileBytes;
-constexpr int kPOff = kVOff + kStages * kTileBytes;
-constexpr int kBarOff = kPOff + kTileBytes;
+constexpr int kBarOff = kVOff + kStages * kTileBytes;
 // barrier slots (8 bytes each)
-constexpr int kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKvEmpty = 5, kBarS = 7, kBarP = 8,
-              kBarO = 9, kNumBars = 10;
+constexpr int kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKvEmpty = 5, kBarS = 7, kBarP = 9,
+              kBarO = 11, kNumBars = 13;
 constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
 constexpr int kAbortOff = kTmemSlotOff + 8;
 constexpr int kSmemBytes = kAbortOff + 8 + 1024;  // + slack for 1024-byte alignment
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;            // S: columns 0-127, O: 128-255
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;            // S0, S1, O0, O1: 128 columns each
 constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, 0, 0);  // A=Q K-major, B=K K-major
-constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, 0, 1);   // A=P K-major, B=V MN-major
+constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, 0, 1);   // A=P (TMEM), B=V MN-major
 constexpr float kLn2 = 0.693147180559945309f;
 
 struct PrefillParams {
@@ -58,7 +67,7 @@ struct PrefillParams {
   __nv_bfloat16 *out;
   float *lse;
   int32_t max_blocks, num_seqs, total_q, max_seqlen_q, max_seqlen_k;
-  int32_t num_q_heads, num_kv_heads, block_size, num_blocks, n_qtiles;
+  int32_t num_q_heads, num_kv_heads, block_size, num_blocks, n_rowtiles;
   float scale_log2;
 };
 
@@ -79,9 +88,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t = p.n_qtiles - 1 - static_cast<int>(blockIdx.x);  // heaviest tiles first
-  const int h = blockIdx.y, s = blockIdx.z;
-  const int g = h / (p.num_q_heads / p.num_kv_heads);
+  const int s = blockIdx.z;
+  const int G = p.num_q_heads / p.num_kv_heads;
 
   // a CTA gave up waiting (in this or an earlier launch): skip the work until
   // the error word is read and cleared; decided once per CTA
@@ -94,18 +102,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (q0 < 0 || Lq < 0 || Lk < Lq || Lq > p.max_seqlen_q || Lk > p.max_seqlen_k ||
       q1 > p.total_q ||
       static_cast<int64_t>(Lk) > static_cast<int64_t>(p.max_blocks) * p.block_size) {
-    if (blockIdx.x == 0 && h == 0 && tid == 0) atomicOr(&g_prefill_errors, kErrSeqlens);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) atomicOr(&g_prefill_errors, kErrSeqlens);
     return;
   }
-  const int row0 = t * kBM;
-  if (row0 >= Lq) return;
-  const int diag = Lk - Lq;                        // query i sees keys <= diag + i
-  const int last_row = min(Lq, row0 + kBM) - 1;
-  const int kv_end = diag + last_row + 1;          // keys this tile needs (<= Lk)
-  const int n_tiles = (kv_end + kBN - 1) / kBN;
+  // the two query tiles: (head, first row) each; heaviest row tiles first
+  const int rt = p.n_rowtiles - 1 - static_cast<int>(blockIdx.x);
+  int head[kTiles], row0[kTiles];
+  if (G >= 2) {
+    head[0] = 2 * blockIdx.y;
+    head[1] = 2 * blockIdx.y + 1;
+    row0[0] = row0[1] = rt * kBM;
+  } else {
+    head[0] = head[1] = blockIdx.y;
+    row0[0] = 2 * rt * kBM + kBM;  // the later (heavier) row tile first
+    row0[1] = 2 * rt * kBM;
+  }
+  const int g = head[0] / G;
+  const int diag = Lk - Lq;  // query i sees keys <= diag + i
+  int n_tiles[kTiles];
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t) {
+    if (row0[t] >= Lq) {
+      n_tiles[t] = 0;
+    } else {
+      const int kv_end = diag + min(Lq, row0[t] + kBM);  // keys this tile needs (<= Lk)
+      n_tiles[t] = (kv_end + kBN - 1) / kBN;
+    }
+  }
+  const int n_max = max(n_tiles[0], n_tiles[1]);
+  if (n_max == 0) return;
 
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + kQOff, sK = sbase + kKOff, sV = sbase + kVOff, sP = sbase + kPOff;
+  const uint32_t sQ = sbase + kQOff, sK = sbase + kKOff, sV = sbase + kVOff;
   const uint32_t bars = sbase + kBarOff;
   auto bar = [&](int i) { return bars + 8u * i; };
   volatile int *abort = reinterpret_cast<volatile int *>(smem + kAbortOff);
@@ -117,13 +145,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarVFull + i), 1);
       mbar_init(bar(kBarKvEmpty + i), 1);
     }
-    mbar_init(bar(kBarS), 1);
-    mbar_init(bar(kBarP), kBM);
-    mbar_init(bar(kBarO), 1);
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(bar(kBarS + t), 1);
+      mbar_init(bar(kBarP + t), kBM);
+      mbar_init(bar(kBarO + t), 1);
+    }
     *abort = 0;
     fence_barrier_init();
   }
-  if (warp == 4) {
+  if (warp == 0) {
     tmem_alloc(sbase + kTmemSlotOff, kTmemCols);
     tmem_relinquish();
   }
@@ -131,19 +161,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kTmemSlotOff);
-  const uint32_t tS = tmem, tO = tmem + kBN;
 
-  if (warp == 4) {
+  if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tensormap(&q_map);
       prefetch_tensormap(&k_map);
       prefetch_tensormap(&v_map);
-      mbar_arrive_expect_tx(bar(kBarQ), kTileBytes);
-      tma_load_3d(sQ, &q_map, bar(kBarQ), 0, h, q0 + row0);
-      tma_load_3d(sQ + kHalfBytes, &q_map, bar(kBarQ), 64, h, q0 + row0);
+      uint32_t qbytes = 0;
+#pragma unroll
+      for (int t = 0; t < kTiles; ++t) qbytes += n_tiles[t] > 0 ? kTileBytes : 0;
+      mbar_arrive_expect_tx(bar(kBarQ), qbytes);
+#pragma unroll
+      for (int t = 0; t < kTiles; ++t) {
+        if (n_tiles[t] == 0) continue;
+        tma_load_3d(sQ + t * kTileBytes, &q_map, bar(kBarQ), 0, head[t], q0 + row0[t]);
+        tma_load_3d(sQ + t * kTileBytes + kHalfBytes, &q_map, bar(kBarQ), 64, head[t],
+                    q0 + row0[t]);
+      }
       const int64_t table = static_cast<int64_t>(s) * p.max_blocks;
-      for (int j = 0; j < n_tiles; ++j) {
+      for (int j = 0; j < n_max; ++j) {
         const int st = j & 1;
         if (j >= kStages && !wait_(bar(kBarKvEmpty + st), ((j >> 1) - 1) & 1, abort)) {
           fail(abort);
@@ -185,89 +222,105 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     bool good = __all_sync(0xffffffffu, wait_(bar(kBarQ), 0, abort));
-    auto issue_s = [&](int j) -> bool {
+    int v_ready = -1;  // last KV tile whose V is resident (and tail-zeroed)
+    auto issue_s = [&](int t, int j) -> bool {
       const int st = j & 1;
       if (!__all_sync(0xffffffffu, wait_(bar(kBarKFull + st), (j >> 1) & 1, abort)))
         return false;
       tc_fence_after();
       if (lane == 0) {
+        const uint32_t tS = tmem + t * kBN;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_bf16_ss(tS, smem_desc_sw128(sQ + off, 16, 1024),
+          mma_bf16_ss(tS, smem_desc_sw128(sQ + t * kTileBytes + off, 16, 1024),
                       smem_desc_sw128(sK + st * kTileBytes + off, 16, 1024), kIdescQK, kk > 0);
         }
-        mma_commit(bar(kBarS));
+        mma_commit(bar(kBarS + t));
       }
       __syncwarp();
       return true;
     };
-    auto issue_pv = [&](int j) -> bool {
+    auto issue_pv = [&](int t, int j) -> bool {
       const int st = j & 1;
-      if (!__all_sync(0xffffffffu, wait_(bar(kBarVFull + st), (j >> 1) & 1, abort)))
-        return false;
-      const int r0 = Lk - j * kBN;  // V rows >= r0 are past the segment's last key
-      if (r0 < kBN) {
-        const uint32_t vbase = sV + st * kTileBytes;
-        const int n16 = (kBN - r0) * 16;  // 16-byte pieces over both column halves
-        for (int idx = lane; idx < n16; idx += 32) {
-          const int row = r0 + idx / 16, piece = idx % 16;
-          const uint32_t addr = vbase + (piece / 8) * kHalfBytes + row * 128 + (piece % 8) * 16;
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(0u), "r"(0u), "r"(0u),
-                       "r"(0u)
-                       : "memory");
+      if (v_ready != j) {
+        if (!__all_sync(0xffffffffu, wait_(bar(kBarVFull + st), (j >> 1) & 1, abort)))
+          return false;
+        const int r0 = Lk - j * kBN;  // V rows >= r0 are past the segment's last key
+        if (r0 < kBN) {
+          const uint32_t vbase = sV + st * kTileBytes;
+          const int n16 = (kBN - r0) * 16;  // 16-byte pieces over both column halves
+          for (int idx = lane; idx < n16; idx += 32) {
+            const int row = r0 + idx / 16, piece = idx % 16;
+            const uint32_t addr = vbase + (piece / 8) * kHalfBytes + row * 128 + (piece % 8) * 16;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(0u),
+                         "r"(0u), "r"(0u), "r"(0u)
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
         }
-        fence_proxy_async_smem();
-        __syncwarp();
+        v_ready = j;
       }
+      // P_t(j) is in TMEM once the softmax of tile t has arrived
+      if (!__all_sync(0xffffffffu, wait_(bar(kBarP + t), j & 1, abort))) return false;
       tc_fence_after();
       if (lane == 0) {
+        const uint32_t tP = tmem + t * kBN;             // P over the first 64 columns of S_t
+        const uint32_t tO = tmem + 2 * kBN + t * kD;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t poff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_bf16_ss(tO, smem_desc_sw128(sP + poff, 16, 1024),
+          mma_bf16_ts(tO, tP + kk * 8,
                       smem_desc_sw128(sV + st * kTileBytes + kk * 16 * 128, kHalfBytes, 1024),
                       kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(bar(kBarO));
-        mma_commit(bar(kBarKvEmpty + st));
+        mma_commit(bar(kBarO + t));
       }
       __syncwarp();
       return true;
     };
-    if (good) good = issue_s(0);
-    for (int j = 1; good && j < n_tiles; ++j) {
-      good = __all_sync(0xffffffffu, wait_(bar(kBarP), (j - 1) & 1, abort)) &&
-             issue_s(j) && issue_pv(j - 1);
+    for (int t = 0; good && t < kTiles; ++t)
+      if (n_tiles[t] > 0) good = issue_s(t, 0);
+    for (int j = 1; good && j <= n_max; ++j) {
+      // finish tile j-1 for every query tile, starting tile j where needed
+      for (int t = 0; good && t < kTiles; ++t) {
+        if (j - 1 >= n_tiles[t]) continue;
+        good = issue_pv(t, j - 1);
+        if (good && j < n_tiles[t]) good = issue_s(t, j);
+      }
+      if (good && lane == 0) mma_commit(bar(kBarKvEmpty + ((j - 1) & 1)));
+      __syncwarp();
     }
-    if (good)
-      good = __all_sync(0xffffffffu, wait_(bar(kBarP), (n_tiles - 1) & 1, abort)) &&
-             issue_pv(n_tiles - 1);
     if (!good && lane == 0) fail(abort);
   } else {
     // ------------------------------------------------------------ softmax / epilogue
-    const int r = tid;                      // row within the tile == TMEM lane
-    const int qi = row0 + r;                // query index within the segment
+    const int t = (warp - 2) / 4;           // query tile of this warpgroup
+    const int quad = warp & 3;              // TMEM lane quadrant this warp may access
+    const int r = quad * 32 + lane;         // row within the tile == TMEM lane
+    const int n_t = n_tiles[t];
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + t * kBN + lane_off;
+    const uint32_t tO = tmem + 2 * kBN + t * kD + lane_off;
+    const int qi = row0[t] + r;             // query index within the segment
     const int lim = diag + qi;              // last key this row may see
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     float m = -INFINITY, l = 0.f;
     bool good = true;
     uint32_t x[kBN];
-    for (int j = 0; j < n_tiles; ++j) {
-      if (!__all_sync(0xffffffffu, wait_(bar(kBarS), j & 1, abort))) {
+    for (int j = 0; j < n_t; ++j) {
+      if (!__all_sync(0xffffffffu, wait_(bar(kBarS + t), j & 1, abort))) {
         good = false;
         break;
       }
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c)
-        tmem_ld32(tS + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
+        tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
       tmem_wait_ld();
       const int kbase = j * kBN;
-      const bool need_mask = (kbase + kBN - 1 > diag + row0) || (kbase + kBN > Lk);
+      const bool need_mask = (kbase + kBN - 1 > diag + row0[t]) || (kbase + kBN > Lk);
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < kBN; ++c) {
@@ -276,63 +329,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         x[c] = __float_as_uint(v);
         mx = fmaxf(mx, v);
       }
-      const float m_new = fmaxf(m, mx);
-      const float alpha = fast_exp2(m - m_new);
+      // a row whose maximum grew rescales its O row (its P.V up to tile j-1 is
+      // complete, since S_t(j) was issued after it); the TMEM accesses are
+      // warp-wide, so the warp does it when any of its rows needs it. Keeping
+      // the exact running maximum makes the largest probability exactly 1,
+      // which bf16 holds without rounding.
+      if (j == 0) {
+        m = mx;
+      } else if (__any_sync(0xffffffffu, mx > m)) {
+        const float m_new = fmaxf(m, mx);
+        const float alpha = fast_exp2(m - m_new);
+#pragma unroll 1
+        for (int c = 0; c < kD / 16; ++c) {
+          uint32_t o[16];
+          tmem_ld16(tO + c * 16, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st16(tO + c * 16, o);
+        }
+        tmem_wait_st();
+        l *= alpha;
+        m = m_new;
+      }
+      // probabilities, packed two per word in place: word c (read 2c, 2c+1
+      // first) lands in x[c], which is no longer needed
       float rowsum = 0.f;
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        const float pr = fast_exp2(__uint_as_float(x[c]) - m_new);
-        rowsum += pr;
-        x[c] = __float_as_uint(pr);
+      for (int c = 0; c < kBN / 2; ++c) {
+        const float p0 = fast_exp2(__uint_as_float(x[2 * c]) - m);
+        const float p1 = fast_exp2(__uint_as_float(x[2 * c + 1]) - m);
+        rowsum += p0 + p1;
+        x[c] = pack_bf16x2(p0, p1);
       }
-      l = l * alpha + rowsum;
-      m = m_new;
-      if (j > 0) {
-        // P.V of the previous tile must be done: it reads the P buffer and
-        // accumulates into the O row that is rescaled here
-        if (!__all_sync(0xffffffffu, wait_(bar(kBarO), (j - 1) & 1, abort))) {
-          good = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int c = 0; c < kD / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + lane_off + c * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + lane_off + c * 32, o);
-          }
-          tmem_wait_st();
-        }
-      }
-      // P row -> shared memory, K-major with the 128-byte swizzle
-#pragma unroll
-      for (int ch = 0; ch < kBN / 8; ++ch) {
-        const uint32_t w0 = pack_bf16x2(__uint_as_float(x[ch * 8 + 0]), __uint_as_float(x[ch * 8 + 1]));
-        const uint32_t w1 = pack_bf16x2(__uint_as_float(x[ch * 8 + 2]), __uint_as_float(x[ch * 8 + 3]));
-        const uint32_t w2 = pack_bf16x2(__uint_as_float(x[ch * 8 + 4]), __uint_as_float(x[ch * 8 + 5]));
-        const uint32_t w3 = pack_bf16x2(__uint_as_float(x[ch * 8 + 6]), __uint_as_float(x[ch * 8 + 7]));
-        const uint32_t addr = sP + (ch >> 3) * kHalfBytes + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1),
-                     "r"(w2), "r"(w3)
-                     : "memory");
-      }
-      fence_proxy_async_smem();
+      l += rowsum;
+      // P (bf16, two per column) over the first 64 columns of S_t
+      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(kBarP));
+      mbar_arrive(bar(kBarP + t));
     }
-    if (__all_sync(0xffffffffu, good && wait_(bar(kBarO), (n_tiles - 1) & 1, abort))) {
+    if (n_t > 0 &&
+        __all_sync(0xffffffffu, good && wait_(bar(kBarO + t), (n_t - 1) & 1, abort))) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool store = qi < Lq;
-      __nv_bfloat16 *orow = p.out + (static_cast<int64_t>(q0 + qi) * p.num_q_heads + h) * kD;
+      __nv_bfloat16 *orow =
+          p.out + (static_cast<int64_t>(q0 + qi) * p.num_q_heads + head[t]) * kD;
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(tO + lane_off + c * 32, o);
+        tmem_ld32(tO + c * 32, o);
         tmem_wait_ld();
         if (store) {
 #pragma unroll
@@ -347,15 +395,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (store && p.lse != nullptr)
-        p.lse[static_cast<int64_t>(q0 + qi) * p.num_q_heads + h] = (m + log2f(l)) * kLn2;
-    } else if (tid == 0) {
+        p.lse[static_cast<int64_t>(q0 + qi) * p.num_q_heads + head[t]] = (m + log2f(l)) * kLn2;
+    } else if (n_t > 0 && r == 0) {
       fail(abort);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -367,6 +415,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
                            const CUtensorMap &k_map, const CUtensorMap &v_map,
                            cudaStream_t stream) {
   if (a.total_q == 0 || a.max_seqlen_q == 0 || a.num_seqs == 0) return cudaSuccess;
+  const int G = a.num_q_heads / a.num_kv_heads;
   PrefillParams p;
   p.cu_q = a.cu_seqlens_q;
   p.cu_k = a.cu_seqlens_k;
@@ -382,12 +431,13 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
   p.num_kv_heads = a.num_kv_heads;
   p.block_size = a.block_size;
   p.num_blocks = a.num_blocks;
-  p.n_qtiles = (a.max_seqlen_q + kBM - 1) / kBM;
+  const int rows_per_cta = G >= 2 ? kBM : 2 * kBM;
+  p.n_rowtiles = (a.max_seqlen_q + rows_per_cta - 1) / rows_per_cta;
   p.scale_log2 = a.scale_log2;
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_qtiles, a.num_q_heads, a.num_seqs);
+  dim3 grid(p.n_rowtiles, G >= 2 ? a.num_q_heads / 2 : a.num_q_heads, a.num_seqs);
   prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(q_map, k_map, v_map, p);
   return cudaGetLastError();
 }

@@ -76,7 +76,7 @@ def test_decode_argument_checks(L):
     assert _decode(L, bs=24) == pkv.PKV_ERR_UNSUPPORTED
     assert _decode(L, scale=float("nan")) == pkv.PKV_ERR_INVALID_ARG
     assert _decode(L, ws=None) == pkv.PKV_ERR_WORKSPACE_TOO_SMALL
-    assert _decode(L, S=4096) == pkv.PKV_ERR_UNSUPPORTED
+    assert _decode(L, S=2048) == pkv.PKV_ERR_UNSUPPORTED
     assert _decode(L, out=ctypes.c_void_p(0x10008)) == pkv.PKV_ERR_INVALID_ARG
 
 
