@@ -239,9 +239,7 @@ class Sweep:
                      ctx=_dev(st.context_lens), out=torch.empty((S, H_q, D), dtype=torch.bfloat16,
                                                                  device="cuda"),
                      lse=torch.empty((S, H_q), dtype=torch.float32, device="cuda"))
-            d["ws"] = torch.empty(pkv.decode_workspace_size(S, H_q, case.H_kv, D,
-                                                            st.max_context_len),
-                                  dtype=torch.uint8, device="cuda")
+            d["ws"] = pkv.new_decode_workspace(S, H_q, case.H_kv, D, st.max_context_len)
             self.layers.append(d)
             self.host_cases.append(case)
         torch.cuda.synchronize()
@@ -253,40 +251,47 @@ class Sweep:
         self.max_ctx = c0.step.max_context_len
         self.scale = c0.scale
 
-    def calls(self, stream_handle):
-        """Per layer: (store_fn, decode_fn) closures over ctypes arguments."""
+    def calls(self, stream_handle, fused=True):
+        """Per layer, the C-ABI calls of one decode step as (function, args) pairs:
+        the fused store+decode call, or the KV store then the decode."""
         P = ctypes.c_void_p
         L = self.L
         out = []
         for d in self.layers:
-            sargs = (P(d["k"].data_ptr()), P(d["v"].data_ptr()), P(d["kc"].data_ptr()),
-                     P(d["vc"].data_ptr()), P(d["slots"].data_ptr()), d["k"].shape[0], self.H_kv,
-                     self.D, self.bs, self.NB, P(stream_handle))
-            dargs = (P(d["q"].data_ptr()), P(d["kc"].data_ptr()), P(d["vc"].data_ptr()),
-                     P(d["bt"].data_ptr()), d["bt"].shape[1], P(d["ctx"].data_ptr()),
-                     self.max_ctx, self.S, self.H_q, self.H_kv, self.D, self.bs, self.NB,
-                     ctypes.c_float(self.scale), P(d["out"].data_ptr()), P(d["lse"].data_ptr()),
-                     P(d["ws"].data_ptr()), d["ws"].numel(), P(stream_handle))
-            out.append((sargs, dargs))
+            common = (P(d["q"].data_ptr()), P(d["kc"].data_ptr()), P(d["vc"].data_ptr()),
+                      P(d["bt"].data_ptr()), d["bt"].shape[1], P(d["ctx"].data_ptr()),
+                      self.max_ctx, self.S, self.H_q, self.H_kv, self.D, self.bs, self.NB,
+                      ctypes.c_float(self.scale), P(d["out"].data_ptr()), P(d["lse"].data_ptr()),
+                      P(d["ws"].data_ptr()), d["ws"].numel(), P(stream_handle))
+            if fused:
+                out.append([(L.pkv_paged_decode_attn_store,
+                             (P(d["k"].data_ptr()), P(d["v"].data_ptr()),
+                              P(d["slots"].data_ptr())) + common)])
+            else:
+                out.append([(L.pkv_kv_store,
+                             (P(d["k"].data_ptr()), P(d["v"].data_ptr()), P(d["kc"].data_ptr()),
+                              P(d["vc"].data_ptr()), P(d["slots"].data_ptr()), d["k"].shape[0],
+                              self.H_kv, self.D, self.bs, self.NB, P(stream_handle))),
+                            (L.pkv_paged_decode_attn, common)])
         return out
 
     def run_step(self, calls, events=None):
+        """Issue one step; with events, bracket each layer's last (decode) call."""
         L = self.L
-        for i, (sargs, dargs) in enumerate(calls):
-            if L.pkv_kv_store(*sargs) != 0:
-                raise RuntimeError("pkv_kv_store failed")
-            if events is not None:
-                events[i][0].record()
-            if L.pkv_paged_decode_attn(*dargs) != 0:
-                raise RuntimeError("pkv_paged_decode_attn failed: " +
-                                   L.pkv_last_cuda_error().decode())
-            if events is not None:
-                events[i][1].record()
+        for i, layer in enumerate(calls):
+            for j, (fn, args) in enumerate(layer):
+                last = j == len(layer) - 1
+                if events is not None and last:
+                    events[i][0].record()
+                if fn(*args) != 0:
+                    raise RuntimeError("pkv call failed: " + L.pkv_last_cuda_error().decode())
+                if events is not None and last:
+                    events[i][1].record()
 
 
-def time_sweep(sweep, steps, warmup, device):
+def time_sweep(sweep, steps, warmup, device, fused=True):
     stream = torch.cuda.current_stream()
-    calls = sweep.calls(stream.cuda_stream)
+    calls = sweep.calls(stream.cuda_stream, fused)
     for _ in range(warmup):
         sweep.run_step(calls)
     torch.cuda.synchronize()
@@ -306,17 +311,17 @@ def time_sweep(sweep, steps, warmup, device):
     return total_ms, decode_ms
 
 
-def time_sweep_graph(sweep, steps, warmup):
+def time_sweep_graph(sweep, steps, warmup, fused=True):
     """The same step captured once into a CUDA graph and replayed."""
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        calls = sweep.calls(s.cuda_stream)
+        calls = sweep.calls(s.cuda_stream, fused)
         sweep.run_step(calls)  # warm the stream before capture
         s.synchronize()
         with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
-            sweep.run_step(sweep.calls(s.cuda_stream))
+            sweep.run_step(sweep.calls(s.cuda_stream, fused))
     torch.cuda.synchronize()
     for _ in range(warmup):
         g.replay()
@@ -347,9 +352,9 @@ def time_e2e(sweep, steps, warmup):
         for d, h, stg, (ho, hl) in zip(sweep.layers, hosts, staging, outs):
             for k in ("q", "k", "v", "slots"):
                 stg[k].copy_(h[k], non_blocking=True)
-            pkv.kv_store(stg["k"], stg["v"], d["kc"], d["vc"], stg["slots"])
-            pkv.paged_decode_attn(stg["q"], d["kc"], d["vc"], d["bt"], d["ctx"], sweep.max_ctx,
-                                  sweep.scale, out=d["out"], lse=d["lse"], workspace=d["ws"])
+            pkv.paged_decode_attn_store(stg["k"], stg["v"], stg["slots"], stg["q"], d["kc"],
+                                        d["vc"], d["bt"], d["ctx"], sweep.max_ctx, sweep.scale,
+                                        out=d["out"], lse=d["lse"], workspace=d["ws"])
             ho.copy_(d["out"], non_blocking=True)
             hl.copy_(d["lse"], non_blocking=True)
 
@@ -530,6 +535,7 @@ def main(argv=None):
     peaks = load_peaks()
     layers = args.layers
     value_graph = value_eager = t_max = g_max = None
+    unfused = None
     roofline = None
     e2e = None
     clocks_result = None
@@ -540,6 +546,9 @@ def main(argv=None):
             total_ms, decode_ms = time_sweep(sweep, args.steps, args.warmup, local)
         clocks_result = clocks.result
         graph_ms = time_sweep_graph(sweep, args.steps, args.warmup)
+        # the same step as two calls per layer (KV store, then decode)
+        _, unfused_dec_ms = time_sweep(sweep, args.steps, args.warmup, local, fused=False)
+        unfused_graph_ms = time_sweep_graph(sweep, args.steps, args.warmup, fused=False)
         if pkv.check_device_errors() != 0:
             raise RuntimeError("device error during the timed region")
         t_max = max_over_ranks(total_ms / 1000.0, device="cuda")
@@ -547,19 +556,23 @@ def main(argv=None):
         units = sum_over_ranks(args.steps * layers * DECODE_SEQS, device="cuda")
         value_eager = units / t_max
         value_graph = units / g_max
-        dec_bytes = decode_algorithmic_bytes(DECODE_SEQS, DECODE_CTX)
+        dec_bytes = (decode_algorithmic_bytes(DECODE_SEQS, DECODE_CTX) +
+                     kv_store_algorithmic_bytes(DECODE_SEQS))
         dec_s = statistics.mean(decode_ms) / 1000.0
         achieved = dec_bytes / dec_s / 1e9
         digest = source_digest("decode.cu", "ptx.cuh")
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                     "traffic": profiled_traffic("decode_split", digest),
-                    "kernel": "decode_kernel (persistent split-K with in-kernel merge)",
+                    "kernel": "decode_kernel, fused KV store + split-K decode",
                     "algorithmic_bytes_per_launch": dec_bytes,
                     "us_per_launch": dec_s * 1e6,
                     "peak_kind": f"HBM copy ({peaks['source']})",
                     "source_digest": digest}
-        launches_per_step = layers * 2  # KV store + decode (plus a counter memset)
+        launches_per_step = layers  # one fused store+decode kernel per layer
+        unfused = {"value": units / max_over_ranks(unfused_graph_ms / 1000.0, device="cuda"),
+                   "decode_us_per_call": statistics.mean(unfused_dec_ms) * 1000.0,
+                   "launches_per_step": layers * 2}
         if not args.no_e2e:
             n_e2e = max(args.steps // 4, 10)
             e_ms, h2d, d2h = time_e2e(sweep, n_e2e, args.warmup)
@@ -600,8 +613,8 @@ def main(argv=None):
             "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": f"decode sweep c=64: 64 seqs x ctx 640, {layers} distinct "
-                                   "layer caches, bs=256, 16 q / 8 kv heads x 128, KV store + "
-                                   "decode per layer",
+                                   "layer caches, bs=256, 16 q / 8 kv heads x 128, KV store of "
+                                   "the new token + decode per layer (one fused call)",
                        "timing": "CUDA graph of one step, replayed",
                        "l2": f"inputs larger than L2 ({layers * 168.3 / 1000:.1f} GB of K/V per "
                              "step, 168 MB per layer)",
@@ -609,6 +622,7 @@ def main(argv=None):
                        "decode_ctas": args.decode_ctas, "decode_variant": args.decode_variant},
             "eager": ({"value": value_eager, "ms_per_step": 1000.0 * t_max / args.steps}
                       if t_max else None),
+            "unfused": unfused,
             "roofline": roofline,
             "prefill": prefill,
             "cpu_baseline": cpu,

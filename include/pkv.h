@@ -107,8 +107,10 @@ pkv_status pkv_kv_store(const void *k, const void *v, void *k_cache, void *v_cac
  * are split between warps; its size depends on the number of sequences and
  * heads and on the device's SM count, not on context length. The caller
  * allocates it once and may reuse it for every call with sizes no larger than
- * these; it needs no initialisation (the counters are zeroed on the stream by
- * every call).
+ * these. It must be zero-filled once before its first use (e.g. with
+ * cudaMemsetAsync); every call leaves it ready for the next one. After a call
+ * that raised PKV_DEVERR_TIMEOUT, zero it again. Calls that share a workspace
+ * must be ordered (same stream).
  */
 size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t max_context_len);
@@ -142,10 +144,35 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
                                  size_t workspace_bytes, void *stream);
 
 /*
+ * Fused decode step: the KV store of each sequence's new token and paged decode
+ * attention in one kernel (the engine's per-layer decode work, one launch).
+ * Equivalent to pkv_kv_store(k_new, v_new, k_cache, v_cache, slot_mapping,
+ * num_seqs, ...) followed by pkv_paged_decode_attn(...) on the same stream:
+ * the new token of sequence s is the one at logical position
+ * context_lens[s] - 1, its K/V rows k_new[s], v_new[s] are written to
+ * slot_mapping[s] (-1: not written) and used as that key by the attention.
+ *   k_new, v_new   device bf16 [num_seqs, num_kv_heads, head_dim]
+ *   slot_mapping   device int32 [num_seqs]
+ * Other arguments, the workspace and the error behaviour are those of
+ * pkv_paged_decode_attn; an invalid slot raises PKV_DEVERR_SLOT (not written;
+ * the attention still uses the new rows).
+ */
+pkv_status pkv_paged_decode_attn_store(const void *k_new, const void *v_new,
+                                       const int32_t *slot_mapping, const void *q,
+                                       void *k_cache, void *v_cache,
+                                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t *context_lens, int32_t max_context_len,
+                                       int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                       int64_t num_blocks, float scale, void *out, float *lse,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Tuning knob of the decode launch, process-wide (not thread-safe against
  * concurrent launches): ctas = number of persistent CTAs (0 = one per SM, the
- * default); variant = launch shape (0 = default, three TMA stages per CTA;
- * 1 = two stages). Results do not depend on either, beyond rounding.
+ * default); variant = launch shape (0 = default: three TMA stages per CTA where
+ * they fit in shared memory; 1 = two stages). Results do not depend on either,
+ * beyond rounding.
  * A non-default ctas changes pkv_decode_workspace_size.
  */
 void pkv_decode_set_config(int32_t ctas, int32_t variant);

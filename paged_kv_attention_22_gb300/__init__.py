@@ -70,6 +70,9 @@ def lib():
     L.pkv_paged_decode_attn.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64,
                                         f32, P, P, P, sz, P]
     L.pkv_paged_decode_attn.restype = ctypes.c_int
+    L.pkv_paged_decode_attn_store.argtypes = [P, P, P, P, P, P, P, i32, P, i32, i32, i32, i32,
+                                              i32, i32, i64, f32, P, P, P, sz, P]
+    L.pkv_paged_decode_attn_store.restype = ctypes.c_int
     L.pkv_paged_decode_attn_noalloc.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32,
                                                 i32, i64, f32, P, P, P]
     L.pkv_paged_decode_attn_noalloc.restype = ctypes.c_int
@@ -142,6 +145,15 @@ def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_con
 DECODE_NUM_VARIANTS = 2
 
 
+def new_decode_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                         device="cuda"):
+    """A zero-filled decode workspace (it must start at zero; calls keep it so)."""
+    need = decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len)
+    if need == 0:
+        raise PkvError(PKV_ERR_CUDA, "pkv_decode_workspace_size")
+    return torch.zeros(need, dtype=torch.uint8, device=device)
+
+
 def decode_set_config(ctas: int = 0, variant: int = 0) -> None:
     """Tuning knob of the decode launch: persistent CTAs (0 = one per SM) and
     launch-shape variant (0 = default). Process-wide."""
@@ -165,15 +177,49 @@ def paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, max_conte
         lse = torch.empty((S, H_q), dtype=torch.float32, device=q.device)
     if lse is not None:
         _need(lse, "lse", torch.float32, 2)
-    need = decode_workspace_size(S, H_q, H_kv, D, int(max_context_len))
     if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        workspace = new_decode_workspace(S, H_q, H_kv, D, int(max_context_len), q.device)
     _need(workspace, "workspace", torch.uint8, 1)
     _check(lib().pkv_paged_decode_attn(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
         _ptr(context_lens), int(max_context_len), S, H_q, H_kv, D, bs, NB, float(scale),
         _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)),
         "pkv_paged_decode_attn")
+    return out, lse
+
+
+def paged_decode_attn_store(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
+                            context_lens, max_context_len, scale, out=None, lse=None,
+                            workspace=None, stream=None, with_lse=True):
+    """Fused decode step: store each sequence's new K/V row (position
+    context_lens[s] - 1, slot slot_mapping[s]) and attend. Returns (out, lse)."""
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    S, H_q, D = q.shape
+    NB, bs, H_kv, _ = k_cache.shape
+    if k_new.shape != (S, H_kv, D) or v_new.shape != k_new.shape or slot_mapping.shape[0] != S:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is None and with_lse:
+        lse = torch.empty((S, H_q), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    if workspace is None:
+        workspace = new_decode_workspace(S, H_q, H_kv, D, int(max_context_len), q.device)
+    _need(workspace, "workspace", torch.uint8, 1)
+    _check(lib().pkv_paged_decode_attn_store(
+        _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), int(max_context_len), S,
+        H_q, H_kv, D, bs, NB, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel(), _stream(stream)), "pkv_paged_decode_attn_store")
     return out, lse
 
 

@@ -214,13 +214,19 @@ void pkv_decode_set_config(int32_t ctas, int32_t variant) {
                          std::memory_order_relaxed);
 }
 
-pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
-                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
-                                 const int32_t *context_lens, int32_t max_context_len,
-                                 int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                                 int32_t head_dim, int32_t block_size, int64_t num_blocks,
-                                 float scale, void *out, float *lse, void *workspace,
-                                 size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by the plain and the fused-store decode entry points; k_new == nullptr
+// for the plain one.
+pkv_status decode_common(const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                         const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                         const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
+                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int64_t num_blocks, float scale, void *out,
+                         float *lse, void *workspace, size_t workspace_bytes, void *stream) {
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_tables == nullptr ||
       context_lens == nullptr || out == nullptr)
     return PKV_ERR_INVALID_ARG;
@@ -231,6 +237,7 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
   if (num_seqs > pkv::kDecodeMaxSeqs) return PKV_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PKV_ERR_INVALID_ARG;
+  if (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID_ARG;
   if (workspace == nullptr) return PKV_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned16(workspace)) return PKV_ERR_INVALID_ARG;
   int sms = 0;
@@ -240,6 +247,11 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
   if (workspace_bytes < w.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
 
   pkv::DecodeArgs a;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_cache_w = const_cast<void *>(k_cache);
+  a.v_cache_w = const_cast<void *>(v_cache);
+  a.slot_mapping = slot_mapping;
   a.q = q;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
@@ -260,8 +272,9 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
   a.variant = g_decode_variant.load(std::memory_order_relaxed);
   a.scale_log2 = scale * kLog2e;
 
-  // one box = 16 token rows of a head group (K, V), or the group's q rows
-  CUtensorMap kmap, vmap, qmap;
+  // one box = 16 token rows of a head group (K, V), the group's q rows, or
+  // the group's rows of one new token
+  CUtensorMap kmap, vmap, qmap, knmap, vnmap;
   const int64_t rows = num_blocks * block_size;
   const uint32_t G = static_cast<uint32_t>(num_q_heads / num_kv_heads);
   const uint32_t HG = static_cast<uint32_t>(pkv::decode_group_heads(num_kv_heads));
@@ -274,9 +287,54 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
   if ((st = encode_rows_map(&qmap, q, num_seqs, num_q_heads, head_dim, 128, HG * G, 1, false)) !=
       PKV_OK)
     return st;
-  cudaError_t e = pkv::launch_decode(a, kmap, vmap, qmap, static_cast<cudaStream_t>(stream));
+  if (k_new != nullptr) {
+    if ((st = encode_rows_map(&knmap, k_new, num_seqs, num_kv_heads, head_dim, 128, HG, 1,
+                              false)) != PKV_OK)
+      return st;
+    if ((st = encode_rows_map(&vnmap, v_new, num_seqs, num_kv_heads, head_dim, 128, HG, 1,
+                              false)) != PKV_OK)
+      return st;
+  } else {
+    knmap = qmap;  // unused without the fused store
+    vnmap = qmap;
+  }
+  cudaError_t e =
+      pkv::launch_decode(a, kmap, vmap, qmap, knmap, vnmap, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *context_lens, int32_t max_context_len,
+                                 int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                 float scale, void *out, float *lse, void *workspace,
+                                 size_t workspace_bytes, void *stream) {
+  return decode_common(nullptr, nullptr, nullptr, q, k_cache, v_cache, block_tables,
+                       max_blocks_per_seq, context_lens, max_context_len, num_seqs, num_q_heads,
+                       num_kv_heads, head_dim, block_size, num_blocks, scale, out, lse,
+                       workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_paged_decode_attn_store(const void *k_new, const void *v_new,
+                                       const int32_t *slot_mapping, const void *q,
+                                       void *k_cache, void *v_cache,
+                                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t *context_lens, int32_t max_context_len,
+                                       int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                       int64_t num_blocks, float scale, void *out, float *lse,
+                                       void *workspace, size_t workspace_bytes, void *stream) {
+  if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr) return PKV_ERR_INVALID_ARG;
+  return decode_common(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
+                       max_blocks_per_seq, context_lens, max_context_len, num_seqs, num_q_heads,
+                       num_kv_heads, head_dim, block_size, num_blocks, scale, out, lse,
+                       workspace, workspace_bytes, stream);
 }
 
 size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t max_seqlen_q) {

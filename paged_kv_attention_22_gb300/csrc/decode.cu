@@ -16,8 +16,8 @@
 //
 //   Warps. One producer warp streams the CTA's units through an NS-deep ring of
 //   shared-memory stages (K box, V box and, when a unit opens a segment, the q
-//   rows of the group), each stage freed when all consumer warps are done with
-//   it. Consumer warp g owns KV head g of the group and its G query heads:
+//   rows of the group; with the fused store, the new token's rows), each stage
+//   freed when all consumer warps are done with it. Consumer warp g owns KV head g of the group and its G query heads:
 //   logits with one 8-lane group per key and a transposing butterfly (each
 //   lane ends with one key's logit), online softmax in base 2, then P.V with
 //   half-warps on alternate keys.
@@ -27,8 +27,14 @@
 //   (max, sum, output) partial per CTA in the workspace: a CTA's first segment
 //   goes to slot 2c, its last segment (if different) to slot 2c+1. Each such
 //   warp then bumps the pair's arrival counter, and the last to arrive merges
-//   the partials and writes the row. Nothing waits on another CTA. The counters
-//   are zeroed on the stream right before the kernel.
+//   the partials, writes the row and sets the counter back to zero, so the
+//   counters are zero again after every call. Nothing waits on another CTA.
+//
+//   Fused store. When given the new tokens' K/V rows and slots, the kernel
+//   also writes them into the cache (the producer warps, one sequence per CTA
+//   in turn) and, for the unit that holds a sequence's new token, copies that
+//   token's rows from the inputs over the staged cache row, so the result is
+//   exactly that of storing first and attending after.
 //
 // The 2-wide GQA group makes the logits and P.V skinny matrix-vector products,
 // so the kernel is bound by HBM bandwidth, not by any tensor-core contraction.
@@ -48,6 +54,9 @@ constexpr int kMaxHG = kDecodeMaxGroupHeads;
 constexpr float kLn2 = 0.693147180559945309f;
 
 struct DecodeParams {
+  const uint4 *k_new, *v_new;      // fused store: the new tokens' rows [S, H_kv, D] (or null)
+  uint4 *k_cache_w, *v_cache_w;    // fused store: the caches, written through these
+  const int32_t *slot_mapping;     // fused store: slot of each sequence's new token
   const int32_t *block_tables;
   const int32_t *context_lens;
   __nv_bfloat16 *out;
@@ -68,7 +77,8 @@ template <int G, int NS>
 struct DecodeSmem {
   static constexpr int kKBytes = kChunk * kMaxHG * kRowBytes;     // 32 KiB
   static constexpr int kQBytes = kMaxHG * G * kRowBytes;
-  static constexpr int kStageBytes = 2 * kKBytes + kQBytes;       // K, V, q rows
+  static constexpr int kNewBytes = kMaxHG * kRowBytes;            // new token's K (or V) rows
+  static constexpr int kStageBytes = 2 * kKBytes + kQBytes + 2 * kNewBytes;  // K, V, q, new K, new V
   static constexpr int kProbOffset = NS * kStageBytes;            // float [HG][G][16]
   static constexpr int kProbBytes = kMaxHG * G * kChunk * 4;
   static constexpr int kBarOffset = kProbOffset + kProbBytes;     // u64 full[NS], empty[NS]
@@ -137,7 +147,9 @@ template <int G, int NS>
 __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap k_map,
                   const __grid_constant__ CUtensorMap v_map,
-                  const __grid_constant__ CUtensorMap q_map, const DecodeParams p) {
+                  const __grid_constant__ CUtensorMap q_map,
+                  const __grid_constant__ CUtensorMap kn_map,
+                  const __grid_constant__ CUtensorMap vn_map, const DecodeParams p) {
   using L = DecodeSmem<G, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
@@ -199,39 +211,77 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
   const int n_mine = static_cast<int>(u_hi - u_lo);
   const uint32_t stage0 = smem_u32(smem);
 
+  const bool fused = p.k_new != nullptr;
   if (warp == HG) {
     // ------------------------------------------------------------ producer
+    const uint32_t box = static_cast<uint32_t>(kChunk * HG * kRowBytes);
+    const uint32_t qbox = static_cast<uint32_t>(HG * G * kRowBytes);
+    const uint32_t nbox = static_cast<uint32_t>(HG * kRowBytes);
+    const uint64_t policy = l2_policy_evict_first();
+    Cursor cur = locate(prefix, p.num_seqs, n_groups, u_lo);
+    auto issue = [&](int i) -> bool {
+      const int st = i % NS;
+      if (i >= NS && !mbar_wait(empty0 + 8 * st, ((i / NS) - 1) & 1, &g_decode_errors)) {
+        atomicOr(&g_decode_errors, kErrTimeout);
+        return false;
+      }
+      const uint32_t stage = stage0 + st * L::kStageBytes;
+      const uint32_t bar = full0 + 8 * st;
+      const bool with_q = (i == 0) || (cur.k == 0);
+      const bool with_new = fused && cur.k == chunks_of(prefix, cur.s) - 1;
+      const int key0 = cur.k * kChunk;
+      const int32_t blk =
+          p.block_tables[static_cast<int64_t>(cur.s) * p.max_blocks + key0 / p.block_size];
+      const bool ok = blk >= 0 && blk < p.num_blocks;
+      if (!ok) atomicOr(&g_decode_errors, kErrBlock);
+      mbar_arrive_expect_tx(bar, (ok ? 2 * box : 0) + (with_q ? qbox : 0) +
+                                     (with_new ? 2 * nbox : 0));
+      if (ok) {
+        const int32_t row = blk * p.block_size + key0 % p.block_size;
+        tma_load_3d_hint(stage, &k_map, bar, 0, cur.hg * HG, row, policy);
+        tma_load_3d_hint(stage + L::kKBytes, &v_map, bar, 0, cur.hg * HG, row, policy);
+      }
+      if (with_q) tma_load_3d(stage + 2 * L::kKBytes, &q_map, bar, 0, cur.hg * HG * G, cur.s);
+      if (with_new) {
+        const uint32_t na = stage + 2 * L::kKBytes + L::kQBytes;
+        tma_load_3d(na, &kn_map, bar, 0, cur.hg * HG, cur.s);
+        tma_load_3d(na + L::kNewBytes, &vn_map, bar, 0, cur.hg * HG, cur.s);
+      }
+      advance(cur, prefix, p.num_seqs, n_groups);
+      return true;
+    };
+    bool running = true;
     if (lane == 0) {
       prefetch_tensormap(&k_map);
       prefetch_tensormap(&v_map);
       prefetch_tensormap(&q_map);
-      const uint64_t policy = l2_policy_evict_first();
-      Cursor cur = locate(prefix, p.num_seqs, n_groups, u_lo);
-      const uint32_t box = static_cast<uint32_t>(kChunk * HG * kRowBytes);
-      const uint32_t qbox = static_cast<uint32_t>(HG * G * kRowBytes);
-      for (int i = 0; i < n_mine; ++i) {
-        const int st = i % NS;
-        if (i >= NS && !mbar_wait(empty0 + 8 * st, ((i / NS) - 1) & 1, &g_decode_errors)) {
-          atomicOr(&g_decode_errors, kErrTimeout);
-          break;
+      for (int i = 0; running && i < NS && i < n_mine; ++i) running = issue(i);
+    }
+    if (fused) {
+      // the new tokens' K/V rows go to their cache slots: sequence s is stored
+      // by CTA s mod W, with the whole producer warp
+      const int row_vec = p.num_kv_heads * (kRowBytes / 16);
+      const int64_t num_slots = static_cast<int64_t>(p.num_blocks) * p.block_size;
+      for (int64_t sq = cta; sq < p.num_seqs; sq += W) {
+        const int64_t slot = p.slot_mapping[sq];
+        if (slot == -1) continue;
+        if (slot < -1 || slot >= num_slots) {
+          if (lane == 0) atomicOr(&g_decode_errors, kErrSlot);
+          continue;
         }
-        const uint32_t stage = stage0 + st * L::kStageBytes;
-        const uint32_t bar = full0 + 8 * st;
-        const bool with_q = (i == 0) || (cur.k == 0);
-        const int key0 = cur.k * kChunk;
-        const int32_t blk =
-            p.block_tables[static_cast<int64_t>(cur.s) * p.max_blocks + key0 / p.block_size];
-        const bool ok = blk >= 0 && blk < p.num_blocks;
-        if (!ok) atomicOr(&g_decode_errors, kErrBlock);
-        mbar_arrive_expect_tx(bar, (ok ? 2 * box : 0) + (with_q ? qbox : 0));
-        if (ok) {
-          const int32_t row = blk * p.block_size + key0 % p.block_size;
-          tma_load_3d_hint(stage, &k_map, bar, 0, cur.hg * HG, row, policy);
-          tma_load_3d_hint(stage + L::kKBytes, &v_map, bar, 0, cur.hg * HG, row, policy);
+        for (int idx = lane; idx < row_vec; idx += 32) {
+          p.k_cache_w[slot * row_vec + idx] = p.k_new[sq * row_vec + idx];
+          p.v_cache_w[slot * row_vec + idx] = p.v_new[sq * row_vec + idx];
         }
-        if (with_q) tma_load_3d(stage + 2 * L::kKBytes, &q_map, bar, 0, cur.hg * HG * G, cur.s);
-        advance(cur, prefix, p.num_seqs, n_groups);
       }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      if (running) {
+        prefetch_tensormap(&kn_map);
+        prefetch_tensormap(&vn_map);
+      }
+      for (int i = NS; running && i < n_mine; ++i) running = issue(i);
     }
     return;
   }
@@ -286,6 +336,21 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
       }
     }
     const int nvalid = min(kChunk, ctx - cur.k * kChunk);
+    const bool with_new = fused && cur.k == chunks_of(prefix, cur.s) - 1;
+    if (with_new) {
+      // the unit holds the sequence's new token (key ctx-1): take its K and V
+      // rows from the staged inputs, whatever the cache row held when copied
+      const int r_new = ctx - 1 - cur.k * kChunk;
+      uint8_t *stg = smem + static_cast<size_t>(st) * L::kStageBytes;
+      const uint8_t *na = stg + 2 * L::kKBytes + L::kQBytes;
+      const int part = lane & 15;
+      const int kv = lane >> 4;  // 0: K, 1: V
+      const uint4 row = *reinterpret_cast<const uint4 *>(na + kv * L::kNewBytes + g * kRowBytes +
+                                                         part * 16);
+      *reinterpret_cast<uint4 *>(stg + kv * L::kKBytes + r_new * tok_bytes + g * kRowBytes +
+                                 part * 16) = row;
+      __syncwarp();
+    }
 
     // ---- logits: pass pp covers keys 4*pp + grp; lane group grp, sub-dims sub
     float part[G][4];
@@ -356,7 +421,9 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
         }
       }
     }
-    // this warp is done with the stage (and with prob): release it
+    // this warp is done with the stage (and with prob): release it (after its
+    // own shared-memory writes, if any, are ordered before the next TMA fill)
+    if (with_new) fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * st);
 
@@ -423,8 +490,10 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
         arrived = __shfl_sync(0xffffffffu, arrived, 0);
         if (arrived == static_cast<uint32_t>(wb - wa + 1)) {
           // last piece in: merge the pair's partials. CTA wa holds it in its
-          // last slot unless its range starts at the pair's first unit.
+          // last slot unless its range starts at the pair's first unit. The
+          // counter goes back to zero for the next call.
           __threadfence();
+          if (lane == 0) p.ws_cnt[static_cast<int64_t>(cur.s) * p.num_kv_heads + kvh] = 0u;
           const int64_t wa_slot = 2 * wa + (range_start(wa, W, U) < P0 ? 1 : 0);
 #pragma unroll
           for (int h = 0; h < G; ++h) {
@@ -471,6 +540,7 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
 template <int G, int NS>
 cudaError_t launch_variant(const DecodeArgs &a, const CUtensorMap &k_map,
                            const CUtensorMap &v_map, const CUtensorMap &q_map,
+                           const CUtensorMap &kn_map, const CUtensorMap &vn_map,
                            const DecodeParams &p, cudaStream_t stream) {
   using L = DecodeSmem<G, NS>;
   static_assert(L::total(kDecodeMaxSeqs) <= 227 * 1024, "decode shared memory");
@@ -478,28 +548,33 @@ cudaError_t launch_variant(const DecodeArgs &a, const CUtensorMap &k_map,
   const int smem = L::total(a.num_seqs);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(p.ws_cnt, 0,
-                      sizeof(uint32_t) * static_cast<size_t>(a.num_seqs) * a.num_kv_heads, stream);
-  if (e != cudaSuccess) return e;
-  kern<<<a.grid, (p.hg + 1) * 32, smem, stream>>>(k_map, v_map, q_map, p);
+  kern<<<a.grid, (p.hg + 1) * 32, smem, stream>>>(k_map, v_map, q_map, kn_map, vn_map, p);
   return cudaGetLastError();
 }
 
 template <int G>
 cudaError_t launch_group(const DecodeArgs &a, const CUtensorMap &k_map, const CUtensorMap &v_map,
-                         const CUtensorMap &q_map, const DecodeParams &p, cudaStream_t stream) {
-  static_assert(kDecodeNumVariants == 2, "variant table");
+                         const CUtensorMap &q_map, const CUtensorMap &kn_map,
+                         const CUtensorMap &vn_map, const DecodeParams &p, cudaStream_t stream) {
+  // three stages when they fit in shared memory, else two
+  constexpr int kDefaultStages = DecodeSmem<G, 3>::total(kDecodeMaxSeqs) <= 227 * 1024 ? 3 : 2;
   if (a.variant == 1)
-    return launch_variant<G, kDecodeVariants[1].stages>(a, k_map, v_map, q_map, p, stream);
-  return launch_variant<G, kDecodeVariants[0].stages>(a, k_map, v_map, q_map, p, stream);
+    return launch_variant<G, 2>(a, k_map, v_map, q_map, kn_map, vn_map, p, stream);
+  return launch_variant<G, kDefaultStages>(a, k_map, v_map, q_map, kn_map, vn_map, p, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
                           const CUtensorMap &v_map, const CUtensorMap &q_map,
+                          const CUtensorMap &kn_map, const CUtensorMap &vn_map,
                           cudaStream_t stream) {
   DecodeParams p;
+  p.k_new = static_cast<const uint4 *>(a.k_new);
+  p.v_new = static_cast<const uint4 *>(a.v_new);
+  p.k_cache_w = static_cast<uint4 *>(a.k_cache_w);
+  p.v_cache_w = static_cast<uint4 *>(a.v_cache_w);
+  p.slot_mapping = a.slot_mapping;
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
@@ -518,9 +593,9 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
   p.n_groups = a.num_kv_heads / p.hg;
   p.scale_log2 = a.scale_log2;
   switch (a.num_q_heads / a.num_kv_heads) {
-    case 1: return launch_group<1>(a, k_map, v_map, q_map, p, stream);
-    case 2: return launch_group<2>(a, k_map, v_map, q_map, p, stream);
-    case 4: return launch_group<4>(a, k_map, v_map, q_map, p, stream);
+    case 1: return launch_group<1>(a, k_map, v_map, q_map, kn_map, vn_map, p, stream);
+    case 2: return launch_group<2>(a, k_map, v_map, q_map, kn_map, vn_map, p, stream);
+    case 4: return launch_group<4>(a, k_map, v_map, q_map, kn_map, vn_map, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

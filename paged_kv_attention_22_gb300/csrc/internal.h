@@ -26,13 +26,7 @@ constexpr int kDecodeChunk = 16;          // keys per unit (one TMA box of all h
 constexpr int kDecodeMaxSeqs = 1024;      // sequences per call (chunk prefix lives in smem)
 constexpr int kDecodeMaxGroupHeads = 8;   // KV heads per CTA head group
 
-// Launch shapes of the persistent decode kernel: TMA stages per CTA.
-// Variant 0 is the default.
-struct DecodeVariant {
-  int stages;
-};
-constexpr DecodeVariant kDecodeVariants[] = {{3}, {2}};
-constexpr int kDecodeNumVariants = 2;
+constexpr int kDecodeNumVariants = 2;  // 0: three stages where they fit, 1: two
 
 // KV heads per CTA head group: the largest divisor of H_kv that is <= 8.
 inline int decode_group_heads(int num_kv_heads) {
@@ -42,6 +36,9 @@ inline int decode_group_heads(int num_kv_heads) {
 }
 
 struct DecodeArgs {
+  const void *k_new, *v_new;     // fused store: new rows [S, H_kv, D], or null
+  void *k_cache_w, *v_cache_w;   // fused store: caches to write
+  const int32_t *slot_mapping;   // fused store: slot of each sequence's new token
   const void *q;
   const int32_t *block_tables;
   const int32_t *context_lens;
@@ -49,17 +46,19 @@ struct DecodeArgs {
   float *lse;
   float *ws_o;            // [2 grid, HG, G, D] partial outputs of pieces cut by CTA ranges
   float *ws_ml;           // [2 grid, HG, G, 2] their (max, sum), base 2
-  uint32_t *ws_cnt;       // [S * H_kv] arrival counters (zeroed before the kernel)
+  uint32_t *ws_cnt;       // [S * H_kv] arrival counters at workspace offset 0; zero
+                          // before the first call, and every call leaves them zero
   int32_t max_blocks;
   int32_t max_context_len;
   int32_t num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
   int32_t num_blocks;
   int32_t grid;             // CTAs (persistent; one per SM by default)
-  int32_t variant;          // index into kDecodeVariants
+  int32_t variant;          // launch shape (see kDecodeNumVariants)
   float scale_log2;         // scale * log2(e)
 };
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
                           const CUtensorMap &v_map, const CUtensorMap &q_map,
+                          const CUtensorMap &kn_map, const CUtensorMap &vn_map,
                           cudaStream_t stream);
 cudaError_t take_decode_errors(cudaStream_t stream, uint32_t *flags);
 

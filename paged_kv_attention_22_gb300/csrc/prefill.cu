@@ -306,66 +306,111 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + 2 * kBN + t * kD + lane_off;
     const int qi = row0[t] + r;             // query index within the segment
     const int lim = diag + qi;              // last key this row may see
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;           // running max (log2 units) and sum
     bool good = true;
-    uint32_t x[kBN];
     for (int j = 0; j < n_t; ++j) {
       if (!__all_sync(0xffffffffu, wait_(bar(kBarS + t), j & 1, abort))) {
         good = false;
         break;
       }
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c)
-        tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
-      tmem_wait_ld();
       const int kbase = j * kBN;
+      // keys past the row's causal limit or the segment end are masked; only
+      // the diagonal and the tail tiles have any
       const bool need_mask = (kbase + kBN - 1 > diag + row0[t]) || (kbase + kBN > Lk);
+      const int keep = need_mask ? min(lim, Lk - 1) - kbase + 1 : kBN;  // columns < keep count
+
+      // pass 1: row max of the raw logits (the scale is positive)
       float mx = -INFINITY;
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t x[64];
+        tmem_ld32(tS + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+        tmem_ld32(tS + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+        tmem_wait_ld();
+        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+        if (need_mask) {
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        float v = __uint_as_float(x[c]) * p.scale_log2;
-        if (need_mask && (kbase + c > lim || kbase + c >= Lk)) v = -INFINITY;
-        x[c] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+          for (int c = 0; c < 64; c += 4) {
+            const int cc = hf * 64 + c;
+            a0 = fmaxf(a0, cc + 0 < keep ? __uint_as_float(x[c + 0]) : -INFINITY);
+            a1 = fmaxf(a1, cc + 1 < keep ? __uint_as_float(x[c + 1]) : -INFINITY);
+            a2 = fmaxf(a2, cc + 2 < keep ? __uint_as_float(x[c + 2]) : -INFINITY);
+            a3 = fmaxf(a3, cc + 3 < keep ? __uint_as_float(x[c + 3]) : -INFINITY);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            a0 = fmaxf(a0, __uint_as_float(x[c + 0]));
+            a1 = fmaxf(a1, __uint_as_float(x[c + 1]));
+            a2 = fmaxf(a2, __uint_as_float(x[c + 2]));
+            a3 = fmaxf(a3, __uint_as_float(x[c + 3]));
+          }
+        }
+        mx = fmaxf(mx, fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)));
       }
+      const float mxs = mx * p.scale_log2;  // -inf stays -inf
+
       // a row whose maximum grew rescales its O row (its P.V up to tile j-1 is
       // complete, since S_t(j) was issued after it); the TMEM accesses are
       // warp-wide, so the warp does it when any of its rows needs it. Keeping
       // the exact running maximum makes the largest probability exactly 1,
       // which bf16 holds without rounding.
       if (j == 0) {
-        m = mx;
-      } else if (__any_sync(0xffffffffu, mx > m)) {
-        const float m_new = fmaxf(m, mx);
+        m = mxs;
+      } else if (__any_sync(0xffffffffu, mxs > m)) {
+        const float m_new = fmaxf(m, mxs);
         const float alpha = fast_exp2(m - m_new);
-#pragma unroll 1
-        for (int c = 0; c < kD / 16; ++c) {
-          uint32_t o[16];
-          tmem_ld16(tO + c * 16, o);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t o[64];
+          tmem_ld32(tO + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+          tmem_ld32(tO + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st16(tO + c * 16, o);
+          for (int i = 0; i < 64; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+          tmem_st32(tO + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
         }
         tmem_wait_st();
         l *= alpha;
         m = m_new;
       }
-      // probabilities, packed two per word in place: word c (read 2c, 2c+1
-      // first) lands in x[c], which is no longer needed
-      float rowsum = 0.f;
+
+      // pass 2: P = 2^(x * scale - m), packed two per column over the first 64
+      // columns of S_t (keys 64hf.. land in columns 32hf.., already read)
+      const float neg_m = -m;
+      float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t x[64];
+        tmem_ld32(tS + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+        tmem_ld32(tS + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+        tmem_wait_ld();
+        uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < kBN / 2; ++c) {
-        const float p0 = fast_exp2(__uint_as_float(x[2 * c]) - m);
-        const float p1 = fast_exp2(__uint_as_float(x[2 * c + 1]) - m);
-        rowsum += p0 + p1;
-        x[c] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < 32; c += 2) {
+          const int cc = hf * 64 + 2 * c;
+          float p0 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 0]), p.scale_log2, neg_m));
+          float p1 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 1]), p.scale_log2, neg_m));
+          float p2 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 2]), p.scale_log2, neg_m));
+          float p3 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 3]), p.scale_log2, neg_m));
+          if (need_mask) {
+            p0 = cc + 0 < keep ? p0 : 0.f;
+            p1 = cc + 1 < keep ? p1 : 0.f;
+            p2 = cc + 2 < keep ? p2 : 0.f;
+            p3 = cc + 3 < keep ? p3 : 0.f;
+          }
+          r0 += p0;
+          r1 += p1;
+          r2 += p2;
+          r3 += p3;
+          pk[c] = pack_bf16x2(p0, p1);
+          pk[c + 1] = pack_bf16x2(p2, p3);
+        }
+        tmem_st32(tS + hf * 32, pk);
       }
-      l += rowsum;
-      // P (bf16, two per column) over the first 64 columns of S_t
-      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      l += (r0 + r1) + (r2 + r3);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarP + t));

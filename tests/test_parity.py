@@ -108,15 +108,66 @@ def test_decode_repeated_calls_reuse_the_workspace():
     gpu_store(case.step.new, kc, vc)
     st = case.step
     q, bt, ctx = dev_bf16(st.q), dev_i32(case.block_tables), dev_i32(st.context_lens)
-    ws = torch.empty(pkv.decode_workspace_size(case.num_seqs, case.H_q, case.H_kv, case.D,
-                                               st.max_context_len), dtype=torch.uint8,
-                     device="cuda")
-    for _ in range(3):
+    ws = pkv.new_decode_workspace(case.num_seqs, case.H_q, case.H_kv, case.D, st.max_context_len)
+    for ctas in (0, 5, 0):  # different cuts between CTAs reuse the same counters
+        pkv.decode_set_config(ctas, 0)
         out, lse = pkv.paged_decode_attn(q, kc, vc, bt, ctx, st.max_context_len, case.scale,
                                          workspace=ws)
         assert_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref["out"],
-                     ref["lse"], "repeat")
+                     ref["lse"], f"repeat ctas={ctas}")
+        # every arrival counter is back at zero after the call
+        n_cnt = case.num_seqs * case.H_kv * 4
+        assert int(ws[:n_cnt].view(torch.int32).abs().sum()) == 0
     assert pkv.check_device_errors() == 0
+
+
+def _fused_run(case, kc=None, vc=None):
+    if kc is None:
+        kc, vc = gpu_pool(case)
+        gpu_store(case.history, kc, vc)
+    st = case.step
+    out, lse = pkv.paged_decode_attn_store(
+        dev_bf16(st.new.k), dev_bf16(st.new.v), dev_i32(st.new.slots), dev_bf16(st.q), kc, vc,
+        dev_i32(case.block_tables), dev_i32(st.context_lens), st.max_context_len, case.scale)
+    flags = pkv.check_device_errors()
+    return kc, vc, out.double().cpu().numpy(), lse.double().cpu().numpy(), flags
+
+
+@pytest.mark.parametrize("name", ["tiny/decode", "ragged256/decode", "chain256/decode"])
+def test_fused_store_decode_matches_oracle(name):
+    case = SMALL[name]
+    kc, vc, out, lse, flags = _fused_run(case)
+    ref = oracle_run(case)
+    assert flags == 0
+    assert_cache_equal(kc, vc, ref["kc"], ref["vc"])
+    assert_close(out, lse, ref["out"], ref["lse"], "fused " + name)
+
+
+def test_fused_store_decode_sweep_layer_and_long_context():
+    for case in (W.sweep64_layer(3), W.prefix8k()[1],
+                 W.decode_case("flong", 41, [20000, 1, 17, 333], block_size=16, num_blocks=5200,
+                               blocks_per_seq=1300)):
+        kc, vc, out, lse, flags = _fused_run(case)
+        ref = oracle_run(case)
+        assert flags == 0
+        assert_cache_equal(kc, vc, ref["kc"], ref["vc"])
+        assert_close(out, lse, ref["out"], ref["lse"], "fused " + case.name)
+
+
+def test_fused_store_ignores_stale_cache_row():
+    # the cache row of the new token holds garbage before the call: the
+    # attention must use the new rows, and the row must end up written
+    case = SMALL["ragged256/decode"]
+    kc, vc = gpu_pool(case)
+    gpu_store(case.history, kc, vc)
+    junk = np.full_like(case.step.new.k, 0x4200)  # 32.0 in bf16
+    gpu_store(W.Store(k=junk, v=junk, slots=case.step.new.slots, seq_ids=case.step.new.seq_ids,
+                      positions=case.step.new.positions), kc, vc)
+    kc, vc, out, lse, flags = _fused_run(case, kc, vc)
+    ref = oracle_run(case)
+    assert flags == 0
+    assert_cache_equal(kc, vc, ref["kc"], ref["vc"])
+    assert_close(out, lse, ref["out"], ref["lse"], "fused over stale row")
 
 
 @pytest.mark.parametrize("kind", ["decode", "prefill"])
