@@ -75,6 +75,16 @@ typedef enum {
 #define PKV_DEVERR_SEQLENS 0x8u   /* cu_seqlens inconsistent with the host-side maxima  */
 #define PKV_DEVERR_TIMEOUT 0x10u  /* a kernel gave up waiting on one of its barriers    */
 
+/*
+ * Launch mode, process-wide: with enabled != 0 (the default) every kernel is
+ * launched with programmatic stream serialization (programmatic dependent
+ * launch), so it may start while the previous kernel on the stream finishes;
+ * each kernel still waits for that kernel's completion before it reads or
+ * writes global memory, so results and ordering are unchanged. 0 launches
+ * them the classic way.
+ */
+void pkv_set_programmatic_launch(int32_t enabled);
+
 /* Name of a status code (static string). */
 const char *pkv_status_string(pkv_status status);
 

@@ -76,6 +76,8 @@ def lib():
     L.pkv_paged_decode_attn_noalloc.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32,
                                                 i32, i64, f32, P, P, P]
     L.pkv_paged_decode_attn_noalloc.restype = ctypes.c_int
+    L.pkv_set_programmatic_launch.argtypes = [i32]
+    L.pkv_set_programmatic_launch.restype = None
     L.pkv_decode_set_config.argtypes = [i32, i32]
     L.pkv_decode_set_config.restype = None
     L.pkv_prefill_workspace_size.argtypes = [i32, i32]
@@ -152,6 +154,11 @@ def new_decode_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, max_cont
     if need == 0:
         raise PkvError(PKV_ERR_CUDA, "pkv_decode_workspace_size")
     return torch.zeros(need, dtype=torch.uint8, device=device)
+
+
+def set_programmatic_launch(enabled: bool) -> None:
+    """Launch kernels with programmatic dependent launch (the default) or not."""
+    lib().pkv_set_programmatic_launch(1 if enabled else 0)
 
 
 def decode_set_config(ctas: int = 0, variant: int = 0) -> None:

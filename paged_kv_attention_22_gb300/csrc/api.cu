@@ -102,6 +102,8 @@ pkv_status encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+std::atomic<int32_t> g_pdl{1};
+
 // Tuning overrides of the decode launch (0 = automatic / default).
 std::atomic<int32_t> g_decode_ctas{0};
 std::atomic<int32_t> g_decode_variant{0};
@@ -156,7 +158,15 @@ bool decode_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_
 
 }  // namespace
 
+namespace pkv {
+bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
+}  // namespace pkv
+
 extern "C" {
+
+void pkv_set_programmatic_launch(int32_t enabled) {
+  g_pdl.store(enabled != 0 ? 1 : 0, std::memory_order_relaxed);
+}
 
 const char *pkv_status_string(pkv_status status) {
   switch (status) {

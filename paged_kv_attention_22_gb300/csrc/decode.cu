@@ -31,8 +31,8 @@
 //   counters are zero again after every call. Nothing waits on another CTA.
 //
 //   Fused store. When given the new tokens' K/V rows and slots, the kernel
-//   also writes them into the cache (the producer warps, one sequence per CTA
-//   in turn) and, for the unit that holds a sequence's new token, copies that
+//   also writes them into the cache (a store warp per CTA, one sequence per
+//   CTA in turn) and, for the unit that holds a sequence's new token, copies that
 //   token's rows from the inputs over the staged cache row, so the result is
 //   exactly that of storing first and attending after.
 //
@@ -82,8 +82,9 @@ struct DecodeSmem {
   static constexpr int kProbOffset = NS * kStageBytes;            // float [HG][G][16]
   static constexpr int kProbBytes = kMaxHG * G * kChunk * 4;
   static constexpr int kBarOffset = kProbOffset + kProbBytes;     // u64 full[NS], empty[NS]
-  static constexpr int kPrefixOffset = kBarOffset + 2 * NS * 8;   // int [S + 1] chunk prefix
-  static constexpr int total(int num_seqs) { return kPrefixOffset + 4 * (num_seqs + 1) + 128; }
+  static constexpr int kPrefixOffset = kBarOffset + 2 * NS * 8;   // int [S + 1] chunk prefix,
+                                                                  // then int [S] context lengths
+  static constexpr int total(int num_seqs) { return kPrefixOffset + 4 * (2 * num_seqs + 1) + 128; }
 };
 
 // Position in the unit list: sequence, head group, chunk within the pair.
@@ -144,7 +145,7 @@ __device__ __forceinline__ void butterfly_half(float (&x)[N], bool upper, int la
 }
 
 template <int G, int NS>
-__global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
+__global__ void __launch_bounds__((kMaxHG + 2) * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap k_map,
                   const __grid_constant__ CUtensorMap v_map,
                   const __grid_constant__ CUtensorMap q_map,
@@ -159,14 +160,17 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
   const int HG = p.hg;
   const int n_groups = p.n_groups;
 
+  griddep_wait();  // inputs written by the previous kernel are visible from here on
   // a CTA gave up waiting (in this or an earlier launch): skip the work until
   // the error word is read and cleared; decided once per CTA
   if (__syncthreads_or(threadIdx.x == 0 &&
                        (*reinterpret_cast<volatile uint32_t *>(&g_decode_errors) & kErrTimeout)))
     return;
 
-  // ---- chunk prefix over sequences (invalid lengths count as empty)
+  // ---- chunk prefix over sequences (invalid lengths count as empty) and the
+  // context lengths themselves, kept in shared memory
   int *prefix = reinterpret_cast<int *>(smem + L::kPrefixOffset);
+  int *ctx_of = prefix + p.num_seqs + 1;
   const uint32_t full0 = smem_u32(smem + L::kBarOffset);
   const uint32_t empty0 = full0 + NS * 8;
   if (warp == 0) {
@@ -177,6 +181,7 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
       int n = 0;
       if (s < p.num_seqs) {
         const int ctx = p.context_lens[s];
+        ctx_of[s] = ctx;
         if (ctx <= 0 || ctx > p.max_context_len || ctx > ctx_cap) {
           if (blockIdx.x == 0) atomicOr(&g_decode_errors, kErrContext);
         } else {
@@ -214,52 +219,66 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
   const bool fused = p.k_new != nullptr;
   if (warp == HG) {
     // ------------------------------------------------------------ producer
-    const uint32_t box = static_cast<uint32_t>(kChunk * HG * kRowBytes);
-    const uint32_t qbox = static_cast<uint32_t>(HG * G * kRowBytes);
-    const uint32_t nbox = static_cast<uint32_t>(HG * kRowBytes);
-    const uint64_t policy = l2_policy_evict_first();
-    Cursor cur = locate(prefix, p.num_seqs, n_groups, u_lo);
-    auto issue = [&](int i) -> bool {
-      const int st = i % NS;
-      if (i >= NS && !mbar_wait(empty0 + 8 * st, ((i / NS) - 1) & 1, &g_decode_errors)) {
-        atomicOr(&g_decode_errors, kErrTimeout);
-        return false;
-      }
-      const uint32_t stage = stage0 + st * L::kStageBytes;
-      const uint32_t bar = full0 + 8 * st;
-      const bool with_q = (i == 0) || (cur.k == 0);
-      const bool with_new = fused && cur.k == chunks_of(prefix, cur.s) - 1;
-      const int key0 = cur.k * kChunk;
-      const int32_t blk =
-          p.block_tables[static_cast<int64_t>(cur.s) * p.max_blocks + key0 / p.block_size];
-      const bool ok = blk >= 0 && blk < p.num_blocks;
-      if (!ok) atomicOr(&g_decode_errors, kErrBlock);
-      mbar_arrive_expect_tx(bar, (ok ? 2 * box : 0) + (with_q ? qbox : 0) +
-                                     (with_new ? 2 * nbox : 0));
-      if (ok) {
-        const int32_t row = blk * p.block_size + key0 % p.block_size;
-        tma_load_3d_hint(stage, &k_map, bar, 0, cur.hg * HG, row, policy);
-        tma_load_3d_hint(stage + L::kKBytes, &v_map, bar, 0, cur.hg * HG, row, policy);
-      }
-      if (with_q) tma_load_3d(stage + 2 * L::kKBytes, &q_map, bar, 0, cur.hg * HG * G, cur.s);
-      if (with_new) {
-        const uint32_t na = stage + 2 * L::kKBytes + L::kQBytes;
-        tma_load_3d(na, &kn_map, bar, 0, cur.hg * HG, cur.s);
-        tma_load_3d(na + L::kNewBytes, &vn_map, bar, 0, cur.hg * HG, cur.s);
-      }
-      advance(cur, prefix, p.num_seqs, n_groups);
-      return true;
-    };
-    bool running = true;
     if (lane == 0) {
       prefetch_tensormap(&k_map);
       prefetch_tensormap(&v_map);
       prefetch_tensormap(&q_map);
-      for (int i = 0; running && i < NS && i < n_mine; ++i) running = issue(i);
+      if (fused) {
+        prefetch_tensormap(&kn_map);
+        prefetch_tensormap(&vn_map);
+      }
+      const uint32_t box = static_cast<uint32_t>(kChunk * HG * kRowBytes);
+      const uint32_t qbox = static_cast<uint32_t>(HG * G * kRowBytes);
+      const uint32_t nbox = static_cast<uint32_t>(HG * kRowBytes);
+      const uint64_t policy = l2_policy_evict_first();
+      Cursor cur = locate(prefix, p.num_seqs, n_groups, u_lo);
+      // block-table entry of the unit at `cur`, read one unit ahead
+      auto table_entry = [&](const Cursor &c) {
+        return p.block_tables[static_cast<int64_t>(c.s) * p.max_blocks +
+                              (c.k * kChunk) / p.block_size];
+      };
+      int32_t blk = table_entry(cur);
+      for (int i = 0; i < n_mine; ++i) {
+        const int st = i % NS;
+        Cursor nxt = cur;
+        advance(nxt, prefix, p.num_seqs, n_groups);
+        const int32_t blk_next = (i + 1 < n_mine) ? table_entry(nxt) : 0;
+        if (i >= NS && !mbar_wait(empty0 + 8 * st, ((i / NS) - 1) & 1, &g_decode_errors)) {
+          atomicOr(&g_decode_errors, kErrTimeout);
+          break;
+        }
+        const uint32_t stage = stage0 + st * L::kStageBytes;
+        const uint32_t bar = full0 + 8 * st;
+        const bool with_q = (i == 0) || (cur.k == 0);
+        const bool with_new = fused && cur.k == chunks_of(prefix, cur.s) - 1;
+        const bool ok = blk >= 0 && blk < p.num_blocks;
+        if (!ok) atomicOr(&g_decode_errors, kErrBlock);
+        mbar_arrive_expect_tx(bar, (ok ? 2 * box : 0) + (with_q ? qbox : 0) +
+                                       (with_new ? 2 * nbox : 0));
+        if (ok) {
+          const int32_t row = blk * p.block_size + (cur.k * kChunk) % p.block_size;
+          tma_load_3d_hint(stage, &k_map, bar, 0, cur.hg * HG, row, policy);
+          tma_load_3d_hint(stage + L::kKBytes, &v_map, bar, 0, cur.hg * HG, row, policy);
+        }
+        if (with_q) tma_load_3d(stage + 2 * L::kKBytes, &q_map, bar, 0, cur.hg * HG * G, cur.s);
+        if (with_new) {
+          const uint32_t na = stage + 2 * L::kKBytes + L::kQBytes;
+          tma_load_3d(na, &kn_map, bar, 0, cur.hg * HG, cur.s);
+          tma_load_3d(na + L::kNewBytes, &vn_map, bar, 0, cur.hg * HG, cur.s);
+        }
+        cur = nxt;
+        blk = blk_next;
+      }
+      // every copy of this CTA is issued: the next kernel may start launching
+      griddep_launch_dependents();
     }
+    return;
+  }
+  if (warp == HG + 1) {
+    // ------------------------------------------------------------ store warp
+    // the new tokens' K/V rows go to their cache slots: sequence s is stored by
+    // CTA s mod W (nothing in this launch reads those rows from the cache)
     if (fused) {
-      // the new tokens' K/V rows go to their cache slots: sequence s is stored
-      // by CTA s mod W, with the whole producer warp
       const int row_vec = p.num_kv_heads * (kRowBytes / 16);
       const int64_t num_slots = static_cast<int64_t>(p.num_blocks) * p.block_size;
       for (int64_t sq = cta; sq < p.num_seqs; sq += W) {
@@ -275,17 +294,9 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) {
-      if (running) {
-        prefetch_tensormap(&kn_map);
-        prefetch_tensormap(&vn_map);
-      }
-      for (int i = NS; running && i < n_mine; ++i) running = issue(i);
-    }
     return;
   }
-  if (warp > HG) return;
+  if (warp > HG + 1) return;
 
   // -------------------------------------------------------------- consumers
   const int g = warp;                      // KV head within the group
@@ -313,7 +324,7 @@ __global__ void __launch_bounds__((kMaxHG + 1) * 32, 1)
       return;  // a lost copy: rows of this CTA's range stay unwritten
     }
     if (opens) {
-      ctx = p.context_lens[cur.s];
+      ctx = ctx_of[cur.s];
       seg_first_k = cur.k;
       seg_is_first = (it == 0);
       const uint8_t *qs = kst + 2 * L::kKBytes + g * G * kRowBytes;
@@ -548,8 +559,8 @@ cudaError_t launch_variant(const DecodeArgs &a, const CUtensorMap &k_map,
   const int smem = L::total(a.num_seqs);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<a.grid, (p.hg + 1) * 32, smem, stream>>>(k_map, v_map, q_map, kn_map, vn_map, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(a.grid), dim3((p.hg + 2) * 32), smem, stream, k_map, v_map, q_map,
+                    kn_map, vn_map, p);
 }
 
 template <int G>

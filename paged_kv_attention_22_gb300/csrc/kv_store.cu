@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                     uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                     const int32_t *__restrict__ slot_mapping, int32_t num_tokens,
                     int32_t row_vec, int64_t num_slots) {
+  griddep_wait();  // inputs written by the previous kernel are visible from here on
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warp = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
@@ -75,11 +77,10 @@ cudaError_t launch_kv_store(const KvStoreArgs &a, cudaStream_t stream) {
   if (a.num_tokens == 0) return cudaSuccess;
   const int64_t blocks_needed = (static_cast<int64_t>(a.num_tokens) + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const int grid = static_cast<int>(blocks_needed < 65535 * 8 ? blocks_needed : 65535 * 8);
-  kv_store_kernel<<<grid, kWarpsPerBlock * 32, 0, stream>>>(
-      static_cast<const uint4 *>(a.k), static_cast<const uint4 *>(a.v),
-      static_cast<uint4 *>(a.k_cache), static_cast<uint4 *>(a.v_cache), a.slot_mapping,
-      a.num_tokens, a.row_vec16, a.num_slots);
-  return cudaGetLastError();
+  return launch_pdl(kv_store_kernel, dim3(grid), dim3(kWarpsPerBlock * 32), 0, stream,
+                    static_cast<const uint4 *>(a.k), static_cast<const uint4 *>(a.v),
+                    static_cast<uint4 *>(a.k_cache), static_cast<uint4 *>(a.v_cache),
+                    a.slot_mapping, a.num_tokens, a.row_vec16, a.num_slots);
 }
 
 cudaError_t take_kv_store_errors(cudaStream_t stream, uint32_t *flags) {

@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int s = blockIdx.z;
   const int G = p.num_q_heads / p.num_kv_heads;
 
+  griddep_wait();  // inputs written by the previous kernel are visible from here on
   // a CTA gave up waiting (in this or an earlier launch): skip the work until
   // the error word is read and cleared; decided once per CTA
   if (__syncthreads_or(tid == 0 &&
@@ -221,6 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       rows[b]);
         }
       }
+      // every copy of this CTA is issued: the next kernel may start launching
+      griddep_launch_dependents();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -483,8 +486,8 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_rowtiles, G >= 2 ? a.num_q_heads / 2 : a.num_q_heads, a.num_seqs);
-  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(q_map, k_map, v_map, p);
-  return cudaGetLastError();
+  return launch_pdl(prefill_kernel, grid, dim3(kThreads), kSmemBytes, stream, q_map, k_map, v_map,
+                    p);
 }
 
 cudaError_t take_prefill_errors(cudaStream_t stream, uint32_t *flags) {

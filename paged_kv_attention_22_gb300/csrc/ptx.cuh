@@ -276,6 +276,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the previous kernel on its stream ends.
+// griddep_wait blocks until that kernel has completed and its writes are
+// visible (immediately if there is none); every kernel here calls it before
+// its first global-memory access. griddep_launch_dependents lets the next
+// kernel start launching once every CTA of this one has called it or exited.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- math
 
 // 2^x on the special-function unit (ex2.approx, flushes denormals).

@@ -303,3 +303,17 @@ def test_prefill_bad_seqlens_are_flagged():
                            dev_i32(st.cu_seqlens_k), dev_i32(case.block_tables), 32, 64,
                            case.scale)
     assert pkv.check_device_errors() & pkv.DEVERR_SEQLENS
+
+
+def test_classic_launch_gives_the_same_results():
+    # programmatic dependent launch only changes when kernels may start
+    case = SMALL["ragged256/decode"]
+    pre = SMALL["ragged256/prefill"]
+    a = gpu_run(case), gpu_run(pre)
+    pkv.set_programmatic_launch(False)
+    try:
+        b = gpu_run(case), gpu_run(pre)
+    finally:
+        pkv.set_programmatic_launch(True)
+    for x, y in zip(a, b):
+        assert np.array_equal(x["out"], y["out"]) and np.array_equal(x["lse"], y["lse"])
