@@ -307,8 +307,9 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 1)
   const int half = lane >> 4, vcol = lane & 15;
   float *prob = reinterpret_cast<float *>(smem + L::kProbOffset) + g * G * kChunk;
   Cursor cur = locate(prefix, p.num_seqs, n_groups, u_lo);
-  float qf[G][16];
-  float m[G], lsum[G], o[G][8];
+  uint64_t qf[G][8];  // the lane's 16 query dims per head, as scaled fp32 pairs
+  float m[G], lsum[G];
+  uint64_t o[G][4];   // the lane's 8 output dims per head, as fp32 pairs
   int seg_first_k = 0;
   bool seg_is_first = true;
   int ctx = 0;
@@ -332,18 +333,14 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 1)
       for (int h = 0; h < G; ++h) {
         const uint4 a = *reinterpret_cast<const uint4 *>(qs + h * kRowBytes + sub * 16);
         const uint4 b = *reinterpret_cast<const uint4 *>(qs + h * kRowBytes + 128 + sub * 16);
-        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+        const uint32_t wq[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          qf[h][2 * i] = bf16lo(wa[i]) * p.scale_log2;
-          qf[h][2 * i + 1] = bf16hi(wa[i]) * p.scale_log2;
-          qf[h][8 + 2 * i] = bf16lo(wb[i]) * p.scale_log2;
-          qf[h][8 + 2 * i + 1] = bf16hi(wb[i]) * p.scale_log2;
-        }
+        for (int i = 0; i < 8; ++i)
+          qf[h][i] = f32x2(bf16lo(wq[i]) * p.scale_log2, bf16hi(wq[i]) * p.scale_log2);
         m[h] = -INFINITY;
         lsum[h] = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o[h][i] = 0.f;
+        for (int i = 0; i < 4; ++i) o[h][i] = 0ull;
       }
     }
     const int nvalid = min(kChunk, ctx - cur.k * kChunk);
@@ -371,15 +368,18 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 1)
       const uint4 ka = *reinterpret_cast<const uint4 *>(krow + sub * 16);
       const uint4 kb = *reinterpret_cast<const uint4 *>(krow + 128 + sub * 16);
       const uint32_t wv[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+      uint32_t lo[8], hi[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        lo[i] = wv[i] << 16;
+        hi[i] = wv[i] & 0xFFFF0000u;
+      }
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        float acc = 0.f;
+        uint64_t acc = 0ull;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          acc = fmaf(qf[h][2 * i], bf16lo(wv[i]), acc);
-          acc = fmaf(qf[h][2 * i + 1], bf16hi(wv[i]), acc);
-        }
-        part[h][pp] = acc;
+        for (int i = 0; i < 8; ++i) ffma2(acc, qf[h][i], lo[i], hi[i]);
+        part[h][pp] = f32x2_lo(acc) + f32x2_hi(acc);
       }
     }
     float sc[G];
@@ -402,8 +402,15 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 1)
       const float alpha = fast_exp2(m[h] - m_new);  // 0 on a segment's first unit
       const float pr = fast_exp2(sc[h] - m_new);    // 0 for masked keys
       lsum[h] = lsum[h] * alpha + (counts ? pr : 0.f);
+      if (alpha != 1.f) {
+        const uint64_t a2 = f32x2(alpha, alpha);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[h][i] *= alpha;
+        for (int i = 0; i < 4; ++i) {
+          uint64_t r = 0ull;
+          ffma2(r, a2, static_cast<uint32_t>(o[h][i]), static_cast<uint32_t>(o[h][i] >> 32));
+          o[h][i] = r;
+        }
+      }
       m[h] = m_new;
       if (counts) prob[h * kChunk + my_key] = pr;
     }
@@ -418,17 +425,17 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 1)
         const uint4 vv =
             *reinterpret_cast<const uint4 *>(vst + key * tok_bytes + g * kRowBytes + vcol * 16);
         const uint32_t wv[4] = {vv.x, vv.y, vv.z, vv.w};
-        float pr[G];
+        uint64_t pr2[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) pr[h] = prob[h * kChunk + key];
+        for (int h = 0; h < G; ++h) {
+          const float pr = prob[h * kChunk + key];
+          pr2[h] = f32x2(pr, pr);
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float v0 = bf16lo(wv[i]), v1 = bf16hi(wv[i]);
+          const uint32_t v0 = wv[i] << 16, v1 = wv[i] & 0xFFFF0000u;
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            o[h][2 * i] = fmaf(pr[h], v0, o[h][2 * i]);
-            o[h][2 * i + 1] = fmaf(pr[h], v1, o[h][2 * i + 1]);
-          }
+          for (int h = 0; h < G; ++h) ffma2(o[h][i], pr2[h], v0, v1);
         }
       }
     }
@@ -443,10 +450,16 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 1)
     const bool pair_ends = cur.k == nch - 1;
     if (pair_ends || it == n_mine - 1) {
       float lt[G];
+      float of[G][8];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o[h][i] += __shfl_xor_sync(0xffffffffu, o[h][i], 16);
+        for (int i = 0; i < 4; ++i) {
+          of[h][2 * i] = f32x2_lo(o[h][i]);
+          of[h][2 * i + 1] = f32x2_hi(o[h][i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) of[h][i] += __shfl_xor_sync(0xffffffffu, of[h][i], 16);
         lt[h] = lsum[h];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) lt[h] += __shfl_xor_sync(0xffffffffu, lt[h], off);
@@ -460,10 +473,10 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 1)
           for (int h = 0; h < G; ++h) {
             const float inv = 1.f / lt[h];
             uint4 v;
-            v.x = pack_bf16x2(o[h][0] * inv, o[h][1] * inv);
-            v.y = pack_bf16x2(o[h][2] * inv, o[h][3] * inv);
-            v.z = pack_bf16x2(o[h][4] * inv, o[h][5] * inv);
-            v.w = pack_bf16x2(o[h][6] * inv, o[h][7] * inv);
+            v.x = pack_bf16x2(of[h][0] * inv, of[h][1] * inv);
+            v.y = pack_bf16x2(of[h][2] * inv, of[h][3] * inv);
+            v.z = pack_bf16x2(of[h][4] * inv, of[h][5] * inv);
+            v.w = pack_bf16x2(of[h][6] * inv, of[h][7] * inv);
             *reinterpret_cast<uint4 *>(p.out + (row0 + h) * kD + vcol * 8) = v;
           }
         }
@@ -479,8 +492,8 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 1)
 #pragma unroll
           for (int h = 0; h < G; ++h) {
             float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (base + h) * kD + vcol * 8);
-            __stcg(dst, make_float4(o[h][0], o[h][1], o[h][2], o[h][3]));
-            __stcg(dst + 1, make_float4(o[h][4], o[h][5], o[h][6], o[h][7]));
+            __stcg(dst, make_float4(of[h][0], of[h][1], of[h][2], of[h][3]));
+            __stcg(dst + 1, make_float4(of[h][4], of[h][5], of[h][6], of[h][7]));
           }
         }
         if (lane == 0) {

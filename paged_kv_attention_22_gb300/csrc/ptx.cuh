@@ -305,6 +305,28 @@ __device__ __forceinline__ float fast_exp2(float x) {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Packed fp32 pair math (sm_100+ FFMA2): acc.{lo,hi} = a.{lo,hi} * b.{lo,hi} +
+// acc.{lo,hi}, each rounded as an ordinary fp32 fma. b is given as its two
+// 32-bit halves, typically the two bf16 values of a word widened in place.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(__float_as_uint(lo)), "r"(__float_as_uint(hi)));
+  return r;
+}
+
+__device__ __forceinline__ void ffma2(uint64_t &acc, uint64_t a, uint32_t b_lo, uint32_t b_hi) {
+  asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%1, %2};\n\tfma.rn.f32x2 %0, %3, t, %0;\n\t}"
+      : "+l"(acc)
+      : "r"(b_lo), "r"(b_hi), "l"(a));
+}
+
+__device__ __forceinline__ float f32x2_lo(uint64_t v) {
+  return __uint_as_float(static_cast<uint32_t>(v));
+}
+__device__ __forceinline__ float f32x2_hi(uint64_t v) {
+  return __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
