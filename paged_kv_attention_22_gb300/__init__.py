@@ -144,7 +144,7 @@ def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_con
                                                max_context_len))
 
 
-DECODE_NUM_VARIANTS = 2
+DECODE_NUM_VARIANTS = 3
 
 
 def new_decode_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,

@@ -136,9 +136,9 @@ struct DecodeWorkspace {
   size_t cnt_bytes, ml_offset, o_offset, total;
 };
 
-int32_t decode_grid_ctas(int sms) {
+int32_t decode_grid_ctas(int sms, int variant) {
   const int32_t o = g_decode_ctas.load(std::memory_order_relaxed);
-  return o > 0 ? (o > 65535 ? 65535 : o) : sms;
+  return o > 0 ? (o > 65535 ? 65535 : o) : sms * pkv::decode_variant_ctas_per_sm(variant);
 }
 
 bool decode_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
@@ -146,13 +146,20 @@ bool decode_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       num_q_heads % num_kv_heads != 0)
     return false;
-  const int64_t heads = static_cast<int64_t>(pkv::decode_group_heads(num_kv_heads)) *
-                        (num_q_heads / num_kv_heads);
-  const int64_t slots = 2 * static_cast<int64_t>(decode_grid_ctas(sms));
+  // the largest slots x heads of any launch variant: 2 per CTA, each holding a
+  // head group's G query heads
+  int64_t slot_heads = 0;
+  for (int v = 0; v < pkv::kDecodeNumVariants; ++v) {
+    const int64_t sh = 2 * static_cast<int64_t>(decode_grid_ctas(sms, v)) *
+                       pkv::decode_group_heads(num_kv_heads, pkv::decode_variant_group_max(v));
+    if (sh > slot_heads) slot_heads = sh;
+  }
+  const int64_t G = num_q_heads / num_kv_heads;
   w->cnt_bytes = sizeof(uint32_t) * static_cast<size_t>(num_seqs) * num_kv_heads;
   w->ml_offset = align_up(w->cnt_bytes, 256);
-  w->o_offset = align_up(w->ml_offset + static_cast<size_t>(slots * heads * 2) * sizeof(float), 256);
-  w->total = w->o_offset + static_cast<size_t>(slots * heads * head_dim) * sizeof(float);
+  w->o_offset =
+      align_up(w->ml_offset + static_cast<size_t>(slot_heads * G * 2) * sizeof(float), 256);
+  w->total = w->o_offset + static_cast<size_t>(slot_heads * G * head_dim) * sizeof(float);
   return true;
 }
 
@@ -278,8 +285,8 @@ pkv_status decode_common(const void *k_new, const void *v_new, const int32_t *sl
   a.head_dim = head_dim;
   a.block_size = block_size;
   a.num_blocks = static_cast<int32_t>(num_blocks);
-  a.grid = decode_grid_ctas(sms);
   a.variant = g_decode_variant.load(std::memory_order_relaxed);
+  a.grid = decode_grid_ctas(sms, a.variant);
   a.scale_log2 = scale * kLog2e;
 
   // one box = 16 token rows of a head group (K, V), the group's q rows, or
@@ -287,7 +294,8 @@ pkv_status decode_common(const void *k_new, const void *v_new, const int32_t *sl
   CUtensorMap kmap, vmap, qmap, knmap, vnmap;
   const int64_t rows = num_blocks * block_size;
   const uint32_t G = static_cast<uint32_t>(num_q_heads / num_kv_heads);
-  const uint32_t HG = static_cast<uint32_t>(pkv::decode_group_heads(num_kv_heads));
+  const uint32_t HG = static_cast<uint32_t>(
+      pkv::decode_group_heads(num_kv_heads, pkv::decode_variant_group_max(a.variant)));
   if ((st = encode_rows_map(&kmap, k_cache, rows, num_kv_heads, head_dim, 128, HG,
                             pkv::kDecodeChunk, false)) != PKV_OK)
     return st;

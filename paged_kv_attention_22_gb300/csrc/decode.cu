@@ -50,7 +50,6 @@ namespace {
 constexpr int kD = 128;                 // head dim (the only one supported)
 constexpr int kChunk = kDecodeChunk;    // 16 keys per unit
 constexpr int kRowBytes = kD * 2;       // 256 bytes of one head's K (or V) row
-constexpr int kMaxHG = kDecodeMaxGroupHeads;
 constexpr float kLn2 = 0.693147180559945309f;
 
 struct DecodeParams {
@@ -71,11 +70,11 @@ struct DecodeParams {
   float scale_log2;
 };
 
-// Shared memory layout for G query heads per KV head and NS stages, sized for
-// the largest head group.
-template <int G, int NS>
+// Shared memory layout for G query heads per KV head, head groups of up to
+// kMaxHG KV heads and NS stages.
+template <int G, int kMaxHG, int NS>
 struct DecodeSmem {
-  static constexpr int kKBytes = kChunk * kMaxHG * kRowBytes;     // 32 KiB
+  static constexpr int kKBytes = kChunk * kMaxHG * kRowBytes;     // 32 KiB for 8 heads
   static constexpr int kQBytes = kMaxHG * G * kRowBytes;
   static constexpr int kNewBytes = kMaxHG * kRowBytes;            // new token's K (or V) rows
   static constexpr int kStageBytes = 2 * kKBytes + kQBytes + 2 * kNewBytes;  // K, V, q, new K, new V
@@ -144,14 +143,14 @@ __device__ __forceinline__ void butterfly_half(float (&x)[N], bool upper, int la
   }
 }
 
-template <int G, int NS>
-__global__ void __launch_bounds__((kMaxHG + 2) * 32, 1)
+template <int G, int kMaxHG, int NS>
+__global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
     decode_kernel(const __grid_constant__ CUtensorMap k_map,
                   const __grid_constant__ CUtensorMap v_map,
                   const __grid_constant__ CUtensorMap q_map,
                   const __grid_constant__ CUtensorMap kn_map,
                   const __grid_constant__ CUtensorMap vn_map, const DecodeParams p) {
-  using L = DecodeSmem<G, NS>;
+  using L = DecodeSmem<G, kMaxHG, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                               ~static_cast<uintptr_t>(127));
@@ -561,14 +560,14 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 1)
   }
 }
 
-template <int G, int NS>
+template <int G, int HGM, int NS>
 cudaError_t launch_variant(const DecodeArgs &a, const CUtensorMap &k_map,
                            const CUtensorMap &v_map, const CUtensorMap &q_map,
                            const CUtensorMap &kn_map, const CUtensorMap &vn_map,
                            const DecodeParams &p, cudaStream_t stream) {
-  using L = DecodeSmem<G, NS>;
+  using L = DecodeSmem<G, HGM, NS>;
   static_assert(L::total(kDecodeMaxSeqs) <= 227 * 1024, "decode shared memory");
-  auto kern = decode_kernel<G, NS>;
+  auto kern = decode_kernel<G, HGM, NS>;
   const int smem = L::total(a.num_seqs);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -581,10 +580,14 @@ cudaError_t launch_group(const DecodeArgs &a, const CUtensorMap &k_map, const CU
                          const CUtensorMap &q_map, const CUtensorMap &kn_map,
                          const CUtensorMap &vn_map, const DecodeParams &p, cudaStream_t stream) {
   // three stages when they fit in shared memory, else two
-  constexpr int kDefaultStages = DecodeSmem<G, 3>::total(kDecodeMaxSeqs) <= 227 * 1024 ? 3 : 2;
-  if (a.variant == 1)
-    return launch_variant<G, 2>(a, k_map, v_map, q_map, kn_map, vn_map, p, stream);
-  return launch_variant<G, kDefaultStages>(a, k_map, v_map, q_map, kn_map, vn_map, p, stream);
+  constexpr int kDefaultStages = DecodeSmem<G, 8, 3>::total(kDecodeMaxSeqs) <= 227 * 1024 ? 3 : 2;
+  switch (a.variant) {
+    case 1: return launch_variant<G, 8, 2>(a, k_map, v_map, q_map, kn_map, vn_map, p, stream);
+    case 2: return launch_variant<G, 4, 2>(a, k_map, v_map, q_map, kn_map, vn_map, p, stream);
+    default:
+      return launch_variant<G, 8, kDefaultStages>(a, k_map, v_map, q_map, kn_map, vn_map, p,
+                                                  stream);
+  }
 }
 
 }  // namespace
@@ -613,7 +616,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
   p.num_kv_heads = a.num_kv_heads;
   p.block_size = a.block_size;
   p.num_blocks = a.num_blocks;
-  p.hg = decode_group_heads(a.num_kv_heads);
+  p.hg = decode_group_heads(a.num_kv_heads, decode_variant_group_max(a.variant));
   p.n_groups = a.num_kv_heads / p.hg;
   p.scale_log2 = a.scale_log2;
   switch (a.num_q_heads / a.num_kv_heads) {

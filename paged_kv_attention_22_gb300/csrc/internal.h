@@ -47,11 +47,17 @@ constexpr int kDecodeChunk = 16;          // keys per unit (one TMA box of all h
 constexpr int kDecodeMaxSeqs = 1024;      // sequences per call (chunk prefix lives in smem)
 constexpr int kDecodeMaxGroupHeads = 8;   // KV heads per CTA head group
 
-constexpr int kDecodeNumVariants = 2;  // 0: three stages where they fit, 1: two
+// Launch shapes of the decode kernel (process-wide knob):
+//   0  head groups of up to 8 KV heads, 3 TMA stages where they fit, 1 CTA/SM
+//   1  head groups of up to 8 KV heads, 2 stages, 1 CTA/SM
+//   2  head groups of up to 4 KV heads, 2 stages, 2 CTAs/SM
+constexpr int kDecodeNumVariants = 3;
+inline int decode_variant_group_max(int variant) { return variant == 2 ? 4 : 8; }
+inline int decode_variant_ctas_per_sm(int variant) { return variant == 2 ? 2 : 1; }
 
-// KV heads per CTA head group: the largest divisor of H_kv that is <= 8.
-inline int decode_group_heads(int num_kv_heads) {
-  for (int d = kDecodeMaxGroupHeads; d > 1; --d)
+// KV heads per CTA head group: the largest divisor of H_kv that is <= group_max.
+inline int decode_group_heads(int num_kv_heads, int group_max = kDecodeMaxGroupHeads) {
+  for (int d = group_max; d > 1; --d)
     if (num_kv_heads % d == 0) return d;
   return 1;
 }

@@ -88,7 +88,8 @@ def test_sweep64_layer_full():
     assert_close(got["out"], got["lse"], ref["out"], ref["lse"], "sweep64 layer 0")
 
 
-@pytest.mark.parametrize("ctas,variant", [(1, 0), (2, 0), (7, 0), (1000, 0), (0, 1), (3, 1)])
+@pytest.mark.parametrize("ctas,variant", [(1, 0), (2, 0), (7, 0), (1000, 0), (0, 1), (3, 1),
+                                          (0, 2), (5, 2)])
 def test_decode_launch_shape_does_not_change_results(ctas, variant):
     # the grid decides how pairs are cut between CTAs (1 CTA: whole pairs per
     # CTA; 1000 CTAs: more CTAs than units); the variant decides the stages
