@@ -51,6 +51,7 @@ constexpr int kD = 128;                 // head dim (the only one supported)
 constexpr int kChunk = kDecodeChunk;    // 16 keys per unit
 constexpr int kRowBytes = kD * 2;       // 256 bytes of one head's K (or V) row
 constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kLazyMax = 8.0f;         // log2 units the running max may lag
 
 struct DecodeParams {
   const uint4 *k_new, *v_new;      // fused store: the new tokens' rows [S, H_kv, D] (or null)
@@ -391,17 +392,20 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
       sc[h] = my_key < nvalid ? full : -INFINITY;
     }
 
-    // ---- online softmax over the unit (base 2)
+    // ---- online softmax over the unit (base 2), with a lazy maximum: the
+    // running maximum m only moves (a warp max-reduction and a rescale of the
+    // row's sum and output) when some logit exceeds it by more than 2^8;
+    // otherwise probabilities up to 256 are kept as they are, exact in fp32
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      float mx = sc[h];
+      if (__any_sync(0xffffffffu, sc[h] > m[h] + kLazyMax)) {  // always on a first unit
+        float mx = sc[h];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float m_new = fmaxf(m[h], mx);
-      const float alpha = fast_exp2(m[h] - m_new);  // 0 on a segment's first unit
-      const float pr = fast_exp2(sc[h] - m_new);    // 0 for masked keys
-      lsum[h] = lsum[h] * alpha + (counts ? pr : 0.f);
-      if (alpha != 1.f) {
+        for (int off = 16; off > 0; off >>= 1)
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m_new = fmaxf(m[h], mx);
+        const float alpha = fast_exp2(m[h] - m_new);  // 0 on a segment's first unit
+        lsum[h] *= alpha;
         const uint64_t a2 = f32x2(alpha, alpha);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -409,8 +413,10 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
           ffma2(r, a2, static_cast<uint32_t>(o[h][i]), static_cast<uint32_t>(o[h][i] >> 32));
           o[h][i] = r;
         }
+        m[h] = m_new;
       }
-      m[h] = m_new;
+      const float pr = fast_exp2(sc[h] - m[h]);  // 0 for masked keys
+      lsum[h] += counts ? pr : 0.f;
       if (counts) prob[h * kChunk + my_key] = pr;
     }
     __syncwarp();
