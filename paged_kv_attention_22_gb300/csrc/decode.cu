@@ -25,12 +25,10 @@
 //   Merge. A (sequence, KV head) whose keys all fall in one CTA's range is
 //   finished by that CTA's warp. One cut by range boundaries leaves one
 //   (max, sum, output) partial per CTA in the workspace: a CTA's first segment
-//   goes to slot 2c, its last segment (if different) to slot 2c+1. When a
-//   warp has streamed all its units, it bumps the arrival counter of each of
-//   its cut pairs, and the last piece to arrive merges the partials, writes
-//   the row and sets the counter back to zero, so the counters are zero again
-//   after every call. Nothing waits on another CTA, and no fence or atomic
-//   stalls the stream.
+//   goes to slot 2c, its last segment (if different) to slot 2c+1. Each such
+//   warp then bumps the pair's arrival counter, and the last to arrive merges
+//   the partials, writes the row and sets the counter back to zero, so the
+//   counters are zero again after every call. Nothing waits on another CTA.
 //
 //   Fused store. When given the new tokens' K/V rows and slots, the kernel
 //   also writes them into the cache (a store warp per CTA, one sequence per
@@ -143,72 +141,6 @@ __device__ __forceinline__ void butterfly_half(float (&x)[N], bool upper, int la
     const float send = upper ? x[i] : x[i + N / 2];
     const float keep = upper ? x[i + N / 2] : x[i];
     x[i] = keep + __shfl_xor_sync(0xffffffffu, send, lane_mask);
-  }
-}
-
-// Count this warp's piece of pair (sequence s, KV head hg*HG + g) and, if it is
-// the last piece to arrive, merge every piece's (max, sum, output) partial into
-// the output row and set the pair's counter back to zero. The caller has
-// fenced its own partial stores. CTA c's first piece is in slot 2c, its last
-// in slot 2c+1; the pair's first CTA holds its piece in its last slot unless
-// its range starts at the pair's first unit.
-template <int G>
-__device__ __noinline__ void arrive_and_merge(const DecodeParams &p, const int *prefix,
-                                              int n_groups, int HG, int64_t W, int64_t U, int s,
-                                              int hg, int g, int lane) {
-  const int kvh = hg * HG + g;
-  const int nch = chunks_of(prefix, s);
-  const int64_t cnt = static_cast<int64_t>(s) * p.num_kv_heads + kvh;
-  const int64_t P0 = static_cast<int64_t>(n_groups) * prefix[s] + static_cast<int64_t>(hg) * nch;
-  const int64_t wa = owner_of(P0, W, U), wb = owner_of(P0 + nch - 1, W, U);
-  uint32_t arrived = 0;
-  if (lane == 0) arrived = atomicAdd(p.ws_cnt + cnt, 1u) + 1u;
-  arrived = __shfl_sync(0xffffffffu, arrived, 0);
-  if (arrived != static_cast<uint32_t>(wb - wa + 1)) return;
-  __threadfence();  // every other piece's partial is visible from here on
-  if (lane == 0) p.ws_cnt[cnt] = 0u;
-  const int64_t wa_slot = 2 * wa + (range_start(wa, W, U) < P0 ? 1 : 0);
-  auto part = [&](int64_t x, int h) {  // partial index of CTA x's piece, head h
-    return ((x == wa ? wa_slot : 2 * x) * HG + g) * G + h;
-  };
-  const int64_t row0 = static_cast<int64_t>(s) * p.num_q_heads + kvh * G;
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    // maximum over the pieces (lanes split the pieces)
-    float M = -INFINITY;
-    for (int64_t x = wa + lane; x <= wb; x += 32) M = fmaxf(M, __ldcg(p.ws_ml + part(x, h) * 2));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    // weights, sum and output: 32 pieces at a time, each lane 4 output dims
-    float Lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int64_t base = wa; base <= wb; base += 32) {
-      const int64_t x = base + lane;
-      float f = 0.f;
-      if (x <= wb) {
-        const int64_t i = part(x, h);
-        f = fast_exp2(__ldcg(p.ws_ml + i * 2) - M);
-        Lsum += __ldcg(p.ws_ml + i * 2 + 1) * f;
-      }
-      const int n = static_cast<int>(wb - base + 1 < 32 ? wb - base + 1 : 32);
-#pragma unroll 4
-      for (int j = 0; j < n; ++j) {
-        const float fj = __shfl_sync(0xffffffffu, f, j);
-        const float4 ov =
-            __ldcg(reinterpret_cast<const float4 *>(p.ws_o + part(base + j, h) * kD) + lane);
-        acc[0] = fmaf(ov.x, fj, acc[0]);
-        acc[1] = fmaf(ov.y, fj, acc[1]);
-        acc[2] = fmaf(ov.z, fj, acc[2]);
-        acc[3] = fmaf(ov.w, fj, acc[3]);
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
-    const float inv = 1.f / Lsum;
-    uint2 v;
-    v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    *reinterpret_cast<uint2 *>(p.out + (row0 + h) * kD + lane * 4) = v;
-    if (lane == 0 && p.lse != nullptr) p.lse[row0 + h] = (M + log2f(Lsum)) * kLn2;
   }
 }
 
@@ -381,7 +313,6 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
   int seg_first_k = 0;
   bool seg_is_first = true;
   int ctx = 0;
-  int n_pend = 0, pend_s0 = 0, pend_hg0 = 0, pend_s1 = 0, pend_hg1 = 0;  // cut pieces
 
 #pragma unroll 1
   for (int it = 0; it < n_mine; ++it) {
@@ -577,28 +508,61 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
             __stcg(p.ws_ml + (base + h) * 2 + 1, lt[h]);
           }
         }
-        // counted (and merged, by the last piece to arrive) once the CTA's
-        // units are all done, so the stream is not held up here
-        if (n_pend == 0) {
-          pend_s0 = cur.s;
-          pend_hg0 = cur.hg;
-        } else {
-          pend_s1 = cur.s;
-          pend_hg1 = cur.hg;
+        __threadfence();
+        __syncwarp();
+        const int64_t P0 = static_cast<int64_t>(n_groups) * prefix[cur.s] +
+                           static_cast<int64_t>(cur.hg) * nch;
+        const int64_t wa = owner_of(P0, W, U), wb = owner_of(P0 + nch - 1, W, U);
+        uint32_t arrived = 0;
+        if (lane == 0)
+          arrived = atomicAdd(p.ws_cnt + static_cast<int64_t>(cur.s) * p.num_kv_heads + kvh, 1u) + 1u;
+        arrived = __shfl_sync(0xffffffffu, arrived, 0);
+        if (arrived == static_cast<uint32_t>(wb - wa + 1)) {
+          // last piece in: merge the pair's partials. CTA wa holds it in its
+          // last slot unless its range starts at the pair's first unit. The
+          // counter goes back to zero for the next call.
+          __threadfence();
+          if (lane == 0) p.ws_cnt[static_cast<int64_t>(cur.s) * p.num_kv_heads + kvh] = 0u;
+          const int64_t wa_slot = 2 * wa + (range_start(wa, W, U) < P0 ? 1 : 0);
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float M = -INFINITY;
+            for (int64_t x = wa + lane; x <= wb; x += 32) {
+              const int64_t sl = x == wa ? wa_slot : 2 * x;
+              M = fmaxf(M, __ldcg(p.ws_ml + ((sl * HG + g) * G + h) * 2));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            float Lsum = 0.f;
+            for (int64_t x = wa + lane; x <= wb; x += 32) {
+              const int64_t sl = x == wa ? wa_slot : 2 * x;
+              const int64_t idx = (sl * HG + g) * G + h;
+              Lsum += __ldcg(p.ws_ml + idx * 2 + 1) * fast_exp2(__ldcg(p.ws_ml + idx * 2) - M);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int64_t x = wa; x <= wb; ++x) {
+              const int64_t sl = x == wa ? wa_slot : 2 * x;
+              const int64_t idx = (sl * HG + g) * G + h;
+              const float f = fast_exp2(__ldcg(p.ws_ml + idx * 2) - M);
+              const float4 ov = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + idx * kD) + lane);
+              acc[0] = fmaf(ov.x, f, acc[0]);
+              acc[1] = fmaf(ov.y, f, acc[1]);
+              acc[2] = fmaf(ov.z, f, acc[2]);
+              acc[3] = fmaf(ov.w, f, acc[3]);
+            }
+            const float inv = 1.f / Lsum;
+            uint2 v;
+            v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+            *reinterpret_cast<uint2 *>(p.out + (row0 + h) * kD + lane * 4) = v;
+            if (lane == 0 && p.lse != nullptr) p.lse[row0 + h] = (M + log2f(Lsum)) * kLn2;
+          }
         }
-        ++n_pend;
       }
     }
     advance(cur, prefix, p.num_seqs, n_groups);
-  }
-
-  // ---- arrivals of this warp's cut pieces (at most its first and last)
-  if (n_pend > 0) {
-    // every lane's partial stores are visible before lane 0 counts the arrivals
-    __threadfence();
-    __syncwarp();
-    arrive_and_merge<G>(p, prefix, n_groups, HG, W, U, pend_s0, pend_hg0, g, lane);
-    if (n_pend > 1) arrive_and_merge<G>(p, prefix, n_groups, HG, W, U, pend_s1, pend_hg1, g, lane);
   }
 }
 
