@@ -569,10 +569,10 @@ def main(argv=None):
                     "us_per_launch": dec_s * 1e6,
                     "peak_kind": f"HBM copy ({peaks['source']})",
                     "source_digest": digest}
-        launches_per_step = layers  # one fused store+decode kernel per layer
+        launches_per_step = layers * 2  # fused store+decode kernel and merge kernel
         unfused = {"value": units / max_over_ranks(unfused_graph_ms / 1000.0, device="cuda"),
                    "decode_us_per_call": statistics.mean(unfused_dec_ms) * 1000.0,
-                   "launches_per_step": layers * 2}
+                   "launches_per_step": layers * 3}
         if not args.no_e2e:
             n_e2e = max(args.steps // 4, 10)
             e_ms, h2d, d2h = time_e2e(sweep, n_e2e, args.warmup)

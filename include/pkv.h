@@ -113,14 +113,12 @@ pkv_status pkv_kv_store(const void *k, const void *v, void *k_cache, void *v_cac
 /*
  * Bytes of device workspace that pkv_paged_decode_attn needs for these sizes on
  * the current device (0 on invalid sizes or without a device). The workspace
- * holds per-pair arrival counters and the partial results of pairs whose keys
- * are split between warps; its size depends on the number of sequences and
- * heads and on the device's SM count, not on context length. The caller
+ * holds the partial results of the (sequence, KV head) pairs whose keys are
+ * split between CTAs; its size depends on the heads and on the device's SM
+ * count, not on context length or on the number of sequences. The caller
  * allocates it once and may reuse it for every call with sizes no larger than
- * these. It must be zero-filled once before its first use (e.g. with
- * cudaMemsetAsync); every call leaves it ready for the next one. After a call
- * that raised PKV_DEVERR_TIMEOUT, zero it again. Calls that share a workspace
- * must be ordered (same stream).
+ * these; it needs no initialisation. Calls that share a workspace must be
+ * ordered (same stream).
  */
 size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t max_context_len);

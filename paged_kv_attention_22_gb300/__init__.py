@@ -149,7 +149,7 @@ DECODE_NUM_VARIANTS = 3
 
 def new_decode_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
                          device="cuda"):
-    """A zero-filled decode workspace (it must start at zero; calls keep it so)."""
+    """A decode workspace for these sizes on the current device."""
     need = decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len)
     if need == 0:
         raise PkvError(PKV_ERR_CUDA, "pkv_decode_workspace_size")

@@ -130,10 +130,10 @@ pkv_status check_attention_shape(int32_t num_q_heads, int32_t num_kv_heads, int3
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Decode workspace layout: arrival counters [S * H_kv], then per-CTA partial
-// (max, sum) [2 grid, HG, G, 2] and partial outputs [2 grid, HG, G, D].
+// Decode workspace layout: per-CTA partial (max, sum) [2 grid, HG, G, 2], then
+// partial outputs [2 grid, HG, G, D].
 struct DecodeWorkspace {
-  size_t cnt_bytes, ml_offset, o_offset, total;
+  size_t ml_offset, o_offset, total;
 };
 
 int32_t decode_grid_ctas(int sms, int variant) {
@@ -155,8 +155,7 @@ bool decode_workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_
     if (sh > slot_heads) slot_heads = sh;
   }
   const int64_t G = num_q_heads / num_kv_heads;
-  w->cnt_bytes = sizeof(uint32_t) * static_cast<size_t>(num_seqs) * num_kv_heads;
-  w->ml_offset = align_up(w->cnt_bytes, 256);
+  w->ml_offset = 0;
   w->o_offset =
       align_up(w->ml_offset + static_cast<size_t>(slot_heads * G * 2) * sizeof(float), 256);
   w->total = w->o_offset + static_cast<size_t>(slot_heads * G * head_dim) * sizeof(float);
@@ -274,7 +273,6 @@ pkv_status decode_common(const void *k_new, const void *v_new, const int32_t *sl
   a.context_lens = context_lens;
   a.out = out;
   a.lse = lse;
-  a.ws_cnt = static_cast<uint32_t *>(workspace);
   a.ws_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.ml_offset);
   a.ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + w.o_offset);
   a.max_blocks = max_blocks_per_seq;

@@ -24,11 +24,10 @@
 //
 //   Merge. A (sequence, KV head) whose keys all fall in one CTA's range is
 //   finished by that CTA's warp. One cut by range boundaries leaves one
-//   (max, sum, output) partial per CTA in the workspace: a CTA's first segment
-//   goes to slot 2c, its last segment (if different) to slot 2c+1. Each such
-//   warp then bumps the pair's arrival counter, and the last to arrive merges
-//   the partials, writes the row and sets the counter back to zero, so the
-//   counters are zero again after every call. Nothing waits on another CTA.
+//   (max, sum, output) partial per CTA in the workspace (a CTA's first segment
+//   in slot 2c, its last segment in slot 2c+1), stored with plain stores, and
+//   a small second kernel, launched right behind this one, merges those pairs.
+//   No fence, atomic or wait on another CTA holds up the stream.
 //
 //   Fused store. When given the new tokens' K/V rows and slots, the kernel
 //   also writes them into the cache (a store warp per CTA, one sequence per
@@ -63,7 +62,6 @@ struct DecodeParams {
   float *lse;
   float *ws_o;
   float *ws_ml;
-  uint32_t *ws_cnt;
   int32_t max_blocks, max_context_len, num_seqs, num_q_heads, num_kv_heads, block_size,
       num_blocks;
   int32_t hg;        // KV heads per group (= consumer warps)
@@ -490,7 +488,7 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
           for (int h = 0; h < G; ++h) p.lse[row0 + h] = (m[h] + log2f(lt[h])) * kLn2;
         }
       } else {
-        // a piece of a pair cut by range boundaries: publish the partial
+        // a piece of a pair cut by range boundaries: store the partial
         const int64_t slot = 2 * cta + (seg_is_first ? 0 : 1);
         const int64_t base = (slot * HG + g) * G;  // partial index of head h: base + h
         if (lane < 16) {
@@ -508,61 +506,106 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
             __stcg(p.ws_ml + (base + h) * 2 + 1, lt[h]);
           }
         }
-        __threadfence();
-        __syncwarp();
-        const int64_t P0 = static_cast<int64_t>(n_groups) * prefix[cur.s] +
-                           static_cast<int64_t>(cur.hg) * nch;
-        const int64_t wa = owner_of(P0, W, U), wb = owner_of(P0 + nch - 1, W, U);
-        uint32_t arrived = 0;
-        if (lane == 0)
-          arrived = atomicAdd(p.ws_cnt + static_cast<int64_t>(cur.s) * p.num_kv_heads + kvh, 1u) + 1u;
-        arrived = __shfl_sync(0xffffffffu, arrived, 0);
-        if (arrived == static_cast<uint32_t>(wb - wa + 1)) {
-          // last piece in: merge the pair's partials. CTA wa holds it in its
-          // last slot unless its range starts at the pair's first unit. The
-          // counter goes back to zero for the next call.
-          __threadfence();
-          if (lane == 0) p.ws_cnt[static_cast<int64_t>(cur.s) * p.num_kv_heads + kvh] = 0u;
-          const int64_t wa_slot = 2 * wa + (range_start(wa, W, U) < P0 ? 1 : 0);
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float M = -INFINITY;
-            for (int64_t x = wa + lane; x <= wb; x += 32) {
-              const int64_t sl = x == wa ? wa_slot : 2 * x;
-              M = fmaxf(M, __ldcg(p.ws_ml + ((sl * HG + g) * G + h) * 2));
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            float Lsum = 0.f;
-            for (int64_t x = wa + lane; x <= wb; x += 32) {
-              const int64_t sl = x == wa ? wa_slot : 2 * x;
-              const int64_t idx = (sl * HG + g) * G + h;
-              Lsum += __ldcg(p.ws_ml + idx * 2 + 1) * fast_exp2(__ldcg(p.ws_ml + idx * 2) - M);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int64_t x = wa; x <= wb; ++x) {
-              const int64_t sl = x == wa ? wa_slot : 2 * x;
-              const int64_t idx = (sl * HG + g) * G + h;
-              const float f = fast_exp2(__ldcg(p.ws_ml + idx * 2) - M);
-              const float4 ov = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + idx * kD) + lane);
-              acc[0] = fmaf(ov.x, f, acc[0]);
-              acc[1] = fmaf(ov.y, f, acc[1]);
-              acc[2] = fmaf(ov.z, f, acc[2]);
-              acc[3] = fmaf(ov.w, f, acc[3]);
-            }
-            const float inv = 1.f / Lsum;
-            uint2 v;
-            v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-            v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-            *reinterpret_cast<uint2 *>(p.out + (row0 + h) * kD + lane * 4) = v;
-            if (lane == 0 && p.lse != nullptr) p.lse[row0 + h] = (M + log2f(Lsum)) * kLn2;
-          }
-        }
+        // merged by the merge kernel that follows this one
       }
     }
     advance(cur, prefix, p.num_seqs, n_groups);
+  }
+}
+
+// Chunk prefix over sequences in shared memory, as the decode kernel builds it
+// (invalid lengths count as empty); one warp.
+__device__ __forceinline__ void build_prefix(const DecodeParams &p, int *prefix, int lane) {
+  int carry = 0;
+  const int64_t ctx_cap = static_cast<int64_t>(p.max_blocks) * p.block_size;
+  for (int base = 0; base < p.num_seqs; base += 32) {
+    const int s = base + lane;
+    int n = 0;
+    if (s < p.num_seqs) {
+      const int ctx = p.context_lens[s];
+      if (ctx > 0 && ctx <= p.max_context_len && ctx <= ctx_cap) n = (ctx + kChunk - 1) / kChunk;
+    }
+    int incl = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    if (s < p.num_seqs) prefix[s] = carry + incl - n;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) prefix[p.num_seqs] = carry;
+}
+
+// Merge of the (sequence, KV head) pairs that the decode kernel's CTA ranges
+// cut: one warp per pair, combining the pieces' (max, sum, output) partials.
+// CTA c of the decode kernel stored its first piece in slot 2c, its last in
+// slot 2c+1; the pair's first CTA holds its piece in its last slot unless its
+// range starts at the pair's first unit.
+template <int G>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p, int32_t decode_grid) {
+  extern __shared__ int merge_prefix[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // The partition depends on context lengths only, which the decode kernel
+  // before this one does not write, and every kernel before that one has
+  // completed (the decode kernel waited for it before it let this one
+  // launch): they may be read before the wait below.
+  if (warp == 0) build_prefix(p, merge_prefix, lane);
+  __syncthreads();
+  griddep_launch_dependents();
+  const int HG = p.hg, n_groups = p.n_groups;
+  const int64_t U = static_cast<int64_t>(n_groups) * merge_prefix[p.num_seqs];
+  if (U == 0) return;
+  const int64_t W = decode_grid < U ? decode_grid : U;
+  griddep_wait();  // the decode kernel's partials are visible from here on
+  const int64_t n_pairs = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads;
+  for (int64_t pi = static_cast<int64_t>(blockIdx.x) * 8 + warp; pi < n_pairs;
+       pi += static_cast<int64_t>(gridDim.x) * 8) {
+    const int s = static_cast<int>(pi / p.num_kv_heads), kvh = static_cast<int>(pi % p.num_kv_heads);
+    const int hg = kvh / HG, g = kvh % HG;
+    const int nch = chunks_of(merge_prefix, s);
+    if (nch == 0) continue;
+    const int64_t P0 = static_cast<int64_t>(n_groups) * merge_prefix[s] + static_cast<int64_t>(hg) * nch;
+    const int64_t wa = owner_of(P0, W, U), wb = owner_of(P0 + nch - 1, W, U);
+    if (wa == wb) continue;  // written whole by the decode kernel
+    const int64_t wa_slot = 2 * wa + (range_start(wa, W, U) < P0 ? 1 : 0);
+    auto part = [&](int64_t x, int h) { return ((x == wa ? wa_slot : 2 * x) * HG + g) * G + h; };
+    const int64_t row0 = static_cast<int64_t>(s) * p.num_q_heads + kvh * G;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float M = -INFINITY;
+      for (int64_t x = wa + lane; x <= wb; x += 32) M = fmaxf(M, p.ws_ml[part(x, h) * 2]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      float Lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int64_t base = wa; base <= wb; base += 32) {
+        const int64_t x = base + lane;
+        float f = 0.f;
+        if (x <= wb) {
+          const int64_t i = part(x, h);
+          f = fast_exp2(p.ws_ml[i * 2] - M);
+          Lsum += p.ws_ml[i * 2 + 1] * f;
+        }
+        const int n = static_cast<int>(wb - base + 1 < 32 ? wb - base + 1 : 32);
+#pragma unroll 4
+        for (int j = 0; j < n; ++j) {
+          const float fj = __shfl_sync(0xffffffffu, f, j);
+          const float4 ov = reinterpret_cast<const float4 *>(p.ws_o + part(base + j, h) * kD)[lane];
+          acc[0] = fmaf(ov.x, fj, acc[0]);
+          acc[1] = fmaf(ov.y, fj, acc[1]);
+          acc[2] = fmaf(ov.z, fj, acc[2]);
+          acc[3] = fmaf(ov.w, fj, acc[3]);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
+      const float inv = 1.f / Lsum;
+      uint2 v;
+      v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2 *>(p.out + (row0 + h) * kD + lane * 4) = v;
+      if (lane == 0 && p.lse != nullptr) p.lse[row0 + h] = (M + log2f(Lsum)) * kLn2;
+    }
   }
 }
 
@@ -577,8 +620,13 @@ cudaError_t launch_variant(const DecodeArgs &a, const CUtensorMap &k_map,
   const int smem = L::total(a.num_seqs);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(a.grid), dim3((p.hg + 2) * 32), smem, stream, k_map, v_map, q_map,
-                    kn_map, vn_map, p);
+  e = launch_pdl(kern, dim3(a.grid), dim3((p.hg + 2) * 32), smem, stream, k_map, v_map, q_map,
+                 kn_map, vn_map, p);
+  if (e != cudaSuccess) return e;
+  const int64_t n_pairs = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
+  const int merge_grid = static_cast<int>((n_pairs + 7) / 8);
+  return launch_pdl(decode_merge_kernel<G>, dim3(merge_grid), dim3(256),
+                    sizeof(int) * static_cast<size_t>(a.num_seqs + 1), stream, p, a.grid);
 }
 
 template <int G>
@@ -614,7 +662,6 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
   p.lse = a.lse;
   p.ws_o = a.ws_o;
   p.ws_ml = a.ws_ml;
-  p.ws_cnt = a.ws_cnt;
   p.max_blocks = a.max_blocks;
   p.max_context_len = a.max_context_len;
   p.num_seqs = a.num_seqs;

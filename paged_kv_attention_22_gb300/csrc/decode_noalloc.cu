@@ -55,14 +55,8 @@ extern "C" pkv_status pkv_paged_decode_attn_noalloc(
   void *scratch = nullptr;
   const pkv_status st = scratch_for_current_device(&scratch);
   if (st != PKV_OK) return st;
-  // The arrival counters at the start of the scratch must be zero when the
-  // kernel starts; a successful call leaves them zero, but clearing them here
-  // (on the stream, no allocation) keeps a failed earlier call from leaking
-  // into this one.
-  if (num_seqs > 0 && num_kv_heads > 0 &&
-      cudaMemsetAsync(scratch, 0, sizeof(uint32_t) * static_cast<size_t>(num_seqs) * num_kv_heads,
-                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return PKV_ERR_CUDA;
+  // Nothing in the scratch needs to start at zero: every partial result the
+  // call reads back, it writes first.
   return pkv_paged_decode_attn(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                                max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
                                block_size, num_blocks, scale, out, lse, scratch, kScratchBytes,

@@ -73,8 +73,6 @@ struct DecodeArgs {
   float *lse;
   float *ws_o;            // [2 grid, HG, G, D] partial outputs of pieces cut by CTA ranges
   float *ws_ml;           // [2 grid, HG, G, 2] their (max, sum), base 2
-  uint32_t *ws_cnt;       // [S * H_kv] arrival counters at workspace offset 0; zero
-                          // before the first call, and every call leaves them zero
   int32_t max_blocks;
   int32_t max_context_len;
   int32_t num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;

@@ -110,15 +110,13 @@ def test_decode_repeated_calls_reuse_the_workspace():
     st = case.step
     q, bt, ctx = dev_bf16(st.q), dev_i32(case.block_tables), dev_i32(st.context_lens)
     ws = pkv.new_decode_workspace(case.num_seqs, case.H_q, case.H_kv, case.D, st.max_context_len)
-    for ctas in (0, 5, 0):  # different cuts between CTAs reuse the same counters
+    ws.fill_(255)  # stale contents must not matter
+    for ctas in (0, 5, 0):  # different cuts between CTAs reuse the same workspace
         pkv.decode_set_config(ctas, 0)
         out, lse = pkv.paged_decode_attn(q, kc, vc, bt, ctx, st.max_context_len, case.scale,
                                          workspace=ws)
         assert_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref["out"],
                      ref["lse"], f"repeat ctas={ctas}")
-        # every arrival counter is back at zero after the call
-        n_cnt = case.num_seqs * case.H_kv * 4
-        assert int(ws[:n_cnt].view(torch.int32).abs().sum()) == 0
     assert pkv.check_device_errors() == 0
 
 
