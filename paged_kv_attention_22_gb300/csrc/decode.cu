@@ -51,6 +51,9 @@ constexpr int kChunk = kDecodeChunk;    // 16 keys per unit
 constexpr int kRowBytes = kD * 2;       // 256 bytes of one head's K (or V) row
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kLazyMax = 8.0f;         // log2 units the running max may lag
+constexpr int kMergeFast = 8;            // pieces merged with all loads issued at once
+// warps per merge CTA: small enough for a merge CTA to fit beside a decode CTA
+constexpr int kMergeWarps = 4;
 
 struct DecodeParams {
   const uint4 *k_new, *v_new;      // fused store: the new tokens' rows [S, H_kv, D] (or null)
@@ -543,7 +546,7 @@ __device__ __forceinline__ void build_prefix(const DecodeParams &p, int *prefix,
 // slot 2c+1; the pair's first CTA holds its piece in its last slot unless its
 // range starts at the pair's first unit.
 template <int G>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p, int32_t decode_grid) {
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeParams p, int32_t decode_grid) {
   extern __shared__ int merge_prefix[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // The partition depends on context lengths only, which the decode kernel
@@ -559,8 +562,8 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p,
   const int64_t W = decode_grid < U ? decode_grid : U;
   griddep_wait();  // the decode kernel's partials are visible from here on
   const int64_t n_pairs = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads;
-  for (int64_t pi = static_cast<int64_t>(blockIdx.x) * 8 + warp; pi < n_pairs;
-       pi += static_cast<int64_t>(gridDim.x) * 8) {
+  for (int64_t pi = static_cast<int64_t>(blockIdx.x) * kMergeWarps + warp; pi < n_pairs;
+       pi += static_cast<int64_t>(gridDim.x) * kMergeWarps) {
     const int s = static_cast<int>(pi / p.num_kv_heads), kvh = static_cast<int>(pi % p.num_kv_heads);
     const int hg = kvh / HG, g = kvh % HG;
     const int nch = chunks_of(merge_prefix, s);
@@ -571,6 +574,55 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p,
     const int64_t wa_slot = 2 * wa + (range_start(wa, W, U) < P0 ? 1 : 0);
     auto part = [&](int64_t x, int h) { return ((x == wa ? wa_slot : 2 * x) * HG + g) * G + h; };
     const int64_t row0 = static_cast<int64_t>(s) * p.num_q_heads + kvh * G;
+    const int64_t n = wb - wa + 1;
+    if (n <= kMergeFast) {
+      // every load at once: lane x < n fetches piece x's (max, sum), every
+      // lane its 4 output dims of each piece
+      float mh[G], lh[G];
+      float4 ov[kMergeFast][G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        mh[h] = -INFINITY;
+        lh[h] = 0.f;
+        if (lane < n) {
+          const int64_t i = part(wa + lane, h);
+          mh[h] = p.ws_ml[i * 2];
+          lh[h] = p.ws_ml[i * 2 + 1];
+        }
+      }
+#pragma unroll
+      for (int x = 0; x < kMergeFast; ++x)
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+          ov[x][h] = x < n ? reinterpret_cast<const float4 *>(p.ws_o + part(wa + x, h) * kD)[lane]
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float M = mh[h];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float f = lane < n ? fast_exp2(mh[h] - M) : 0.f;
+        float Lsum = lh[h] * f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int x = 0; x < kMergeFast; ++x) {
+          const float fx = __shfl_sync(0xffffffffu, f, x);
+          acc[0] = fmaf(ov[x][h].x, fx, acc[0]);
+          acc[1] = fmaf(ov[x][h].y, fx, acc[1]);
+          acc[2] = fmaf(ov[x][h].z, fx, acc[2]);
+          acc[3] = fmaf(ov[x][h].w, fx, acc[3]);
+        }
+        const float inv = 1.f / Lsum;
+        uint2 v;
+        v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2 *>(p.out + (row0 + h) * kD + lane * 4) = v;
+        if (lane == 0 && p.lse != nullptr) p.lse[row0 + h] = (M + log2f(Lsum)) * kLn2;
+      }
+      continue;
+    }
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       float M = -INFINITY;
@@ -624,8 +676,8 @@ cudaError_t launch_variant(const DecodeArgs &a, const CUtensorMap &k_map,
                  kn_map, vn_map, p);
   if (e != cudaSuccess) return e;
   const int64_t n_pairs = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
-  const int merge_grid = static_cast<int>((n_pairs + 7) / 8);
-  return launch_pdl(decode_merge_kernel<G>, dim3(merge_grid), dim3(256),
+  const int merge_grid = static_cast<int>((n_pairs + kMergeWarps - 1) / kMergeWarps);
+  return launch_pdl(decode_merge_kernel<G>, dim3(merge_grid), dim3(kMergeWarps * 32),
                     sizeof(int) * static_cast<size_t>(a.num_seqs + 1), stream, p, a.grid);
 }
 
