@@ -563,8 +563,8 @@ def main(argv=None):
         digest = source_digest("decode.cu", "ptx.cuh")
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                    "traffic": profiled_traffic("decode_split", digest),
-                    "kernel": "decode_kernel, fused KV store + split-K decode",
+                    "traffic": profiled_traffic("decode_kernel", digest),
+                    "kernel": "decode call: decode_kernel (fused KV store + split-K) + decode_merge_kernel",
                     "algorithmic_bytes_per_launch": dec_bytes,
                     "us_per_launch": dec_s * 1e6,
                     "peak_kind": f"HBM copy ({peaks['source']})",
