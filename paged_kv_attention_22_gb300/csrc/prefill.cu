@@ -8,11 +8,11 @@
 //
 // One CTA owns two 128-row query tiles that share every K/V tile: with grouped
 // queries (H_q / H_kv >= 2) the two query heads of a head pair over the same
-// 128 rows; without grouping, two consecutive row tiles of one head. 10 warps:
-//   warp 0     TMA producer: both Q tiles once, then K and V tiles of 128 keys
+// 128 rows; without grouping, two consecutive row tiles of one head. 12 warps:
+//   warp 8     TMA producer: both Q tiles once, then K and V tiles of 128 keys
 //              as eight 16-row boxes each (a box never crosses a cache block),
 //              two stages deep, 128-byte swizzled.
-//   warp 1     MMA issuer. TMEM holds S_t (128 fp32 columns) and O_t (128) for
+//   warp 9     MMA issuer. TMEM holds S_t (128 fp32 columns) and O_t (128) for
 //              each tile t. Per KV tile j and query tile t: S_t = Q_t K_j^T
 //              (A and B from shared memory), then, once the softmax has
 //              written P_t (bf16) over the first 64 columns of S_t,
@@ -22,7 +22,7 @@
 //              The V rows past the segment's last key are zeroed before their
 //              first P.V, so stale or poisoned rows never meet a zero
 //              probability.
-//   warps 2-5  softmax of tile 0, warps 6-9 softmax of tile 1: one query row
+//   warps 0-3  softmax of tile 0, warps 4-7 softmax of tile 1: one query row
 //              per thread (TMEM lane = row). Read the S row, mask, online
 //              softmax in base 2 (the O row in TMEM is rescaled only in tiles
 //              where some row's maximum grows), write P back into TMEM; at the
@@ -51,16 +51,24 @@ constexpr int kKOff = kQOff + kTiles * kTileBytes;
 constexpr int kVOff = kKOff + kStages * kTileBytes;
 constexpr int kBarOff = kVOff + kStages * kTileBytes;
 // barrier slots (8 bytes each)
-constexpr int kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKvEmpty = 5, kBarS = 7, kBarP = 9,
-              kBarO = 11, kNumBars = 13;
+constexpr int kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKEmpty = 5, kBarVEmpty = 7, kBarS = 9,
+              kBarP = 11, kBarO = 13, kNumBars = 15;
 constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
 constexpr int kAbortOff = kTmemSlotOff + 8;
 constexpr int kSmemBytes = kAbortOff + 8 + 1024;  // + slack for 1024-byte alignment
-constexpr int kThreads = 320;
+// warps 0-7 softmax (warpgroup t for query tile t), warp 8 TMA producer,
+// warp 9 MMA issuer, warps 10-11 idle: three warpgroups, so that setmaxnreg
+// can move registers from the third to the two softmax warpgroups
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+// registers per thread after the split; 2 * 216 + 72 = 3 * 168, the launch's
+// share per thread of the 64K register file for 384 threads
+constexpr int kSoftmaxRegs = 216, kOtherRegs = 72;
 constexpr uint32_t kTmemCols = 512;            // S0, S1, O0, O1: 128 columns each
 constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, 0, 0);  // A=Q K-major, B=K K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, 0, 1);   // A=P (TMEM), B=V MN-major
 constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kLazyMax = 8.0f;  // log2 units the running maximum may lag
 
 struct PrefillParams {
   const int32_t *cu_q, *cu_k, *block_tables;
@@ -144,7 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(kBarKFull + i), 1);
       mbar_init(bar(kBarVFull + i), 1);
-      mbar_init(bar(kBarKvEmpty + i), 1);
+      mbar_init(bar(kBarKEmpty + i), 1);
+      mbar_init(bar(kBarVEmpty + i), 1);
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(bar(kBarS + t), 1);
@@ -154,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort = 0;
     fence_barrier_init();
   }
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     tmem_alloc(sbase + kTmemSlotOff, kTmemCols);
     tmem_relinquish();
   }
@@ -163,144 +172,169 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kTmemSlotOff);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tensormap(&q_map);
-      prefetch_tensormap(&k_map);
-      prefetch_tensormap(&v_map);
-      uint32_t qbytes = 0;
+  if (warp >= kProducerWarp) {
+    setmaxnreg_dec<kOtherRegs>();
+    if (warp == kProducerWarp) {
+      // ------------------------------------------------------------ TMA producer
+      // Lane b < 8 owns the b-th 16-row box of every KV tile: it reads that
+      // box's block-table entry one tile ahead (the read overlaps the wait
+      // for a free stage) and issues the box's copies; lane 0 arms the
+      // barriers. K and V stages are released separately: K(j) once every
+      // S = Q K(j)^T is done, V(j) once every P.V(j) is.
+      constexpr int kBoxes = kBN / kBoxRows;
+      if (lane == 0) {
+        prefetch_tensormap(&q_map);
+        prefetch_tensormap(&k_map);
+        prefetch_tensormap(&v_map);
+        uint32_t qbytes = 0;
 #pragma unroll
-      for (int t = 0; t < kTiles; ++t) qbytes += n_tiles[t] > 0 ? kTileBytes : 0;
-      mbar_arrive_expect_tx(bar(kBarQ), qbytes);
+        for (int t = 0; t < kTiles; ++t) qbytes += n_tiles[t] > 0 ? kTileBytes : 0;
+        mbar_arrive_expect_tx(bar(kBarQ), qbytes);
 #pragma unroll
-      for (int t = 0; t < kTiles; ++t) {
-        if (n_tiles[t] == 0) continue;
-        tma_load_3d(sQ + t * kTileBytes, &q_map, bar(kBarQ), 0, head[t], q0 + row0[t]);
-        tma_load_3d(sQ + t * kTileBytes + kHalfBytes, &q_map, bar(kBarQ), 64, head[t],
-                    q0 + row0[t]);
+        for (int t = 0; t < kTiles; ++t) {
+          if (n_tiles[t] == 0) continue;
+          tma_load_3d(sQ + t * kTileBytes, &q_map, bar(kBarQ), 0, head[t], q0 + row0[t]);
+          tma_load_3d(sQ + t * kTileBytes + kHalfBytes, &q_map, bar(kBarQ), 64, head[t],
+                      q0 + row0[t]);
+        }
       }
-      const int64_t table = static_cast<int64_t>(s) * p.max_blocks;
+      const int32_t *table = p.block_tables + static_cast<int64_t>(s) * p.max_blocks;
+      auto box_key = [&](int j) { return j * kBN + lane * kBoxRows; };
+      auto has_box = [&](int j) { return lane < kBoxes && j < n_max && box_key(j) < Lk; };
+      int32_t next_blk = has_box(0) ? __ldg(table + box_key(0) / p.block_size) : -1;
+      bool good = true;
       for (int j = 0; j < n_max; ++j) {
         const int st = j & 1;
-        if (j >= kStages && !wait_(bar(kBarKvEmpty + st), ((j >> 1) - 1) & 1, abort)) {
-          fail(abort);
+        const int32_t blk = next_blk;
+        if (has_box(j + 1)) next_blk = __ldg(table + box_key(j + 1) / p.block_size);
+        int32_t row = -1;
+        if (has_box(j)) {
+          if (blk < 0 || blk >= p.num_blocks)
+            atomicOr(&g_prefill_errors, kErrBlock);
+          else
+            row = blk * p.block_size + box_key(j) % p.block_size;
+        }
+        const uint32_t bytes =
+            __popc(__ballot_sync(0xffffffffu, row >= 0)) * 2u * kBoxRows * 128u;
+        if (j >= kStages &&
+            !__all_sync(0xffffffffu, wait_(bar(kBarKEmpty + st), ((j >> 1) - 1) & 1, abort))) {
+          good = false;
           break;
         }
-        int32_t rows[kBN / kBoxRows];
-        uint32_t nbox = 0;
-#pragma unroll
-        for (int b = 0; b < kBN / kBoxRows; ++b) {
-          rows[b] = -1;
-          const int key = j * kBN + b * kBoxRows;
-          if (key < Lk) {
-            const int32_t blk = p.block_tables[table + key / p.block_size];
-            if (blk < 0 || blk >= p.num_blocks) {
-              atomicOr(&g_prefill_errors, kErrBlock);
-            } else {
-              rows[b] = blk * p.block_size + key % p.block_size;
-              ++nbox;
-            }
-          }
+        if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull + st), bytes);
+        __syncwarp();
+        const uint32_t kdst = sK + st * kTileBytes + lane * kBoxRows * 128;
+        if (row >= 0) {
+          tma_load_3d(kdst, &k_map, bar(kBarKFull + st), 0, g, row);
+          tma_load_3d(kdst + kHalfBytes, &k_map, bar(kBarKFull + st), 64, g, row);
         }
-        const uint32_t bytes = nbox * 2u * kBoxRows * 128u;
-        const uint32_t kdst = sK + st * kTileBytes, vdst = sV + st * kTileBytes;
-        mbar_arrive_expect_tx(bar(kBarKFull + st), bytes);
-#pragma unroll
-        for (int b = 0; b < kBN / kBoxRows; ++b) {
-          if (rows[b] < 0) continue;
-          tma_load_3d(kdst + b * kBoxRows * 128, &k_map, bar(kBarKFull + st), 0, g, rows[b]);
-          tma_load_3d(kdst + kHalfBytes + b * kBoxRows * 128, &k_map, bar(kBarKFull + st), 64, g,
-                      rows[b]);
+        if (j >= kStages &&
+            !__all_sync(0xffffffffu, wait_(bar(kBarVEmpty + st), ((j >> 1) - 1) & 1, abort))) {
+          good = false;
+          break;
         }
-        mbar_arrive_expect_tx(bar(kBarVFull + st), bytes);
-#pragma unroll
-        for (int b = 0; b < kBN / kBoxRows; ++b) {
-          if (rows[b] < 0) continue;
-          tma_load_3d(vdst + b * kBoxRows * 128, &v_map, bar(kBarVFull + st), 0, g, rows[b]);
-          tma_load_3d(vdst + kHalfBytes + b * kBoxRows * 128, &v_map, bar(kBarVFull + st), 64, g,
-                      rows[b]);
+        if (lane == 0) mbar_arrive_expect_tx(bar(kBarVFull + st), bytes);
+        __syncwarp();
+        const uint32_t vdst = sV + st * kTileBytes + lane * kBoxRows * 128;
+        if (row >= 0) {
+          tma_load_3d(vdst, &v_map, bar(kBarVFull + st), 0, g, row);
+          tma_load_3d(vdst + kHalfBytes, &v_map, bar(kBarVFull + st), 64, g, row);
         }
       }
       // every copy of this CTA is issued: the next kernel may start launching
-      griddep_launch_dependents();
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    bool good = __all_sync(0xffffffffu, wait_(bar(kBarQ), 0, abort));
-    int v_ready = -1;  // last KV tile whose V is resident (and tail-zeroed)
-    auto issue_s = [&](int t, int j) -> bool {
-      const int st = j & 1;
-      if (!__all_sync(0xffffffffu, wait_(bar(kBarKFull + st), (j >> 1) & 1, abort)))
-        return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t tS = tmem + t * kBN;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_bf16_ss(tS, smem_desc_sw128(sQ + t * kTileBytes + off, 16, 1024),
-                      smem_desc_sw128(sK + st * kTileBytes + off, 16, 1024), kIdescQK, kk > 0);
-        }
-        mma_commit(bar(kBarS + t));
+      if (lane == 0) griddep_launch_dependents();
+      // wait for the last release of each stage, so that no arrival from the
+      // tensor core reaches this CTA's shared memory after it has exited
+      for (int j = max(n_max - kStages, 0); good && j < n_max; ++j) {
+        const uint32_t par = (j >> 1) & 1;
+        good = __all_sync(0xffffffffu, wait_(bar(kBarKEmpty + (j & 1)), par, abort) &&
+                                           wait_(bar(kBarVEmpty + (j & 1)), par, abort));
       }
-      __syncwarp();
-      return true;
-    };
-    auto issue_pv = [&](int t, int j) -> bool {
-      const int st = j & 1;
-      if (v_ready != j) {
-        if (!__all_sync(0xffffffffu, wait_(bar(kBarVFull + st), (j >> 1) & 1, abort)))
+      if (!good && lane == 0) fail(abort);
+    } else if (warp == kMmaWarp) {
+      // ------------------------------------------------------------ MMA issuer
+      bool good = __all_sync(0xffffffffu, wait_(bar(kBarQ), 0, abort));
+      int v_ready = -1;  // last KV tile whose V is resident (and tail-zeroed)
+      auto issue_s = [&](int t, int j) -> bool {
+        const int st = j & 1;
+        if (!__all_sync(0xffffffffu, wait_(bar(kBarKFull + st), (j >> 1) & 1, abort)))
           return false;
-        const int r0 = Lk - j * kBN;  // V rows >= r0 are past the segment's last key
-        if (r0 < kBN) {
-          const uint32_t vbase = sV + st * kTileBytes;
-          const int n16 = (kBN - r0) * 16;  // 16-byte pieces over both column halves
-          for (int idx = lane; idx < n16; idx += 32) {
-            const int row = r0 + idx / 16, piece = idx % 16;
-            const uint32_t addr = vbase + (piece / 8) * kHalfBytes + row * 128 + (piece % 8) * 16;
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(0u),
-                         "r"(0u), "r"(0u), "r"(0u)
-                         : "memory");
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t tS = tmem + t * kBN;
+  #pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+            mma_bf16_ss(tS, smem_desc_sw128(sQ + t * kTileBytes + off, 16, 1024),
+                        smem_desc_sw128(sK + st * kTileBytes + off, 16, 1024), kIdescQK, kk > 0);
           }
-          fence_proxy_async_smem();
-          __syncwarp();
+          mma_commit(bar(kBarS + t));
         }
-        v_ready = j;
-      }
-      // P_t(j) is in TMEM once the softmax of tile t has arrived
-      if (!__all_sync(0xffffffffu, wait_(bar(kBarP + t), j & 1, abort))) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t tP = tmem + t * kBN;             // P over the first 64 columns of S_t
-        const uint32_t tO = tmem + 2 * kBN + t * kD;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          mma_bf16_ts(tO, tP + kk * 8,
-                      smem_desc_sw128(sV + st * kTileBytes + kk * 16 * 128, kHalfBytes, 1024),
-                      kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        __syncwarp();
+        return true;
+      };
+      auto issue_pv = [&](int t, int j) -> bool {
+        const int st = j & 1;
+        if (v_ready != j) {
+          if (!__all_sync(0xffffffffu, wait_(bar(kBarVFull + st), (j >> 1) & 1, abort)))
+            return false;
+          const int r0 = Lk - j * kBN;  // V rows >= r0 are past the segment's last key
+          if (r0 < kBN) {
+            const uint32_t vbase = sV + st * kTileBytes;
+            const int n16 = (kBN - r0) * 16;  // 16-byte pieces over both column halves
+            for (int idx = lane; idx < n16; idx += 32) {
+              const int row = r0 + idx / 16, piece = idx % 16;
+              const uint32_t addr = vbase + (piece / 8) * kHalfBytes + row * 128 + (piece % 8) * 16;
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(0u),
+                           "r"(0u), "r"(0u), "r"(0u)
+                           : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          v_ready = j;
         }
-        mma_commit(bar(kBarO + t));
-      }
+        // P_t(j) is in TMEM once the softmax of tile t has arrived
+        if (!__all_sync(0xffffffffu, wait_(bar(kBarP + t), j & 1, abort))) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t tP = tmem + t * kBN;             // P over the first 64 columns of S_t
+          const uint32_t tO = tmem + 2 * kBN + t * kD;
+  #pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            mma_bf16_ts(tO, tP + kk * 8,
+                        smem_desc_sw128(sV + st * kTileBytes + kk * 16 * 128, kHalfBytes, 1024),
+                        kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(kBarO + t));
+        }
+        __syncwarp();
+        return true;
+      };
+      for (int t = 0; good && t < kTiles; ++t)
+        if (n_tiles[t] > 0) good = issue_s(t, 0);
+      if (good && lane == 0) mma_commit(bar(kBarKEmpty));  // K(0) is free once those are done
       __syncwarp();
-      return true;
-    };
-    for (int t = 0; good && t < kTiles; ++t)
-      if (n_tiles[t] > 0) good = issue_s(t, 0);
-    for (int j = 1; good && j <= n_max; ++j) {
-      // finish tile j-1 for every query tile, starting tile j where needed
-      for (int t = 0; good && t < kTiles; ++t) {
-        if (j - 1 >= n_tiles[t]) continue;
-        good = issue_pv(t, j - 1);
-        if (good && j < n_tiles[t]) good = issue_s(t, j);
+      for (int j = 1; good && j <= n_max; ++j) {
+        // finish tile j-1 for every query tile, starting tile j where needed
+        for (int t = 0; good && t < kTiles; ++t) {
+          if (j - 1 >= n_tiles[t]) continue;
+          good = issue_pv(t, j - 1);
+          if (good && j < n_tiles[t]) good = issue_s(t, j);
+        }
+        // V(j-1) has had its last P.V; K(j) its last S
+        if (good && lane == 0) {
+          mma_commit(bar(kBarVEmpty + ((j - 1) & 1)));
+          if (j < n_max) mma_commit(bar(kBarKEmpty + (j & 1)));
+        }
+        __syncwarp();
       }
-      if (good && lane == 0) mma_commit(bar(kBarKvEmpty + ((j - 1) & 1)));
-      __syncwarp();
+      if (!good && lane == 0) fail(abort);
     }
-    if (!good && lane == 0) fail(abort);
   } else {
+    setmaxnreg_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax / epilogue
-    const int t = (warp - 2) / 4;           // query tile of this warpgroup
+    const int t = warp >> 2;                // query tile of this warpgroup
     const int quad = warp & 3;              // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;         // row within the tile == TMEM lane
     const int n_t = n_tiles[t];
@@ -309,8 +343,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + 2 * kBN + t * kD + lane_off;
     const int qi = row0[t] + r;             // query index within the segment
     const int lim = diag + qi;              // last key this row may see
-    float m = -INFINITY, l = 0.f;           // running max (log2 units) and sum
+    // Running maximum m (log2 units) and two running sums: l of the fp32
+    // probabilities, for the lse, and lr of the same probabilities rounded to
+    // bf16 as the P.V product sees them, which normalises the output. The
+    // maximum is lazy: a row keeps its m until a tile's logits exceed it by
+    // more than kLazyMax, so probabilities stay below 2^kLazyMax and O is
+    // rescaled only when some row of the warp passes that bound. Dividing by
+    // the sum of the rounded probabilities keeps the output a convex
+    // combination of the V rows with the weights the tensor core used, so a
+    // large probability rounded to bf16 costs no more than it does under an
+    // exact maximum.
+    float m = -INFINITY, l = 0.f, lr = 0.f;
     bool good = true;
+    const uint64_t scl = f32x2(p.scale_log2, p.scale_log2);
     for (int j = 0; j < n_t; ++j) {
       if (!__all_sync(0xffffffffu, wait_(bar(kBarS + t), j & 1, abort))) {
         good = false;
@@ -318,102 +363,84 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int kbase = j * kBN;
-      // keys past the row's causal limit or the segment end are masked; only
-      // the diagonal and the tail tiles have any
-      const bool need_mask = (kbase + kBN - 1 > diag + row0[t]) || (kbase + kBN > Lk);
-      const int keep = need_mask ? min(lim, Lk - 1) - kbase + 1 : kBN;  // columns < keep count
-
-      // pass 1: row max of the raw logits (the scale is positive)
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t x[64];
-        tmem_ld32(tS + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-        tmem_ld32(tS + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-        tmem_wait_ld();
-        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
-        if (need_mask) {
+      uint32_t x[kBN];
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) {
-            const int cc = hf * 64 + c;
-            a0 = fmaxf(a0, cc + 0 < keep ? __uint_as_float(x[c + 0]) : -INFINITY);
-            a1 = fmaxf(a1, cc + 1 < keep ? __uint_as_float(x[c + 1]) : -INFINITY);
-            a2 = fmaxf(a2, cc + 2 < keep ? __uint_as_float(x[c + 2]) : -INFINITY);
-            a3 = fmaxf(a3, cc + 3 < keep ? __uint_as_float(x[c + 3]) : -INFINITY);
-          }
-        } else {
+      for (int c = 0; c < kBN; c += 32)
+        tmem_ld32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(&x[c]));
+      tmem_wait_ld();
+      // keys past the row's causal limit or the segment end are masked (their
+      // logit becomes -inf, their probability 0); only the diagonal and the
+      // tail tiles have any
+      if ((kbase + kBN - 1 > diag + row0[t]) || (kbase + kBN > Lk)) {
+        const int keep = min(lim, Lk - 1) - kbase + 1;  // columns < keep are visible
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) {
-            a0 = fmaxf(a0, __uint_as_float(x[c + 0]));
-            a1 = fmaxf(a1, __uint_as_float(x[c + 1]));
-            a2 = fmaxf(a2, __uint_as_float(x[c + 2]));
-            a3 = fmaxf(a3, __uint_as_float(x[c + 3]));
-          }
-        }
-        mx = fmaxf(mx, fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)));
+        for (int c = 0; c < kBN; ++c)
+          if (c >= keep) x[c] = 0xFF800000u;
       }
+      // row max of the raw logits (the scale is positive): eight chains of
+      // three-input maxima
+      float a[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(x[i]);
+#pragma unroll
+      for (int c = 8; c < kBN; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          a[i] = fmax3(a[i], __uint_as_float(x[c + i]), __uint_as_float(x[c + 8 + i]));
+      const float mx = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
       const float mxs = mx * p.scale_log2;  // -inf stays -inf
 
-      // a row whose maximum grew rescales its O row (its P.V up to tile j-1 is
-      // complete, since S_t(j) was issued after it); the TMEM accesses are
-      // warp-wide, so the warp does it when any of its rows needs it. Keeping
-      // the exact running maximum makes the largest probability exactly 1,
-      // which bf16 holds without rounding.
       if (j == 0) {
-        m = mxs;
-      } else if (__any_sync(0xffffffffu, mxs > m)) {
+        m = mxs;  // every row sees key 0, so this is finite
+      } else if (__any_sync(0xffffffffu, mxs > m + kLazyMax)) {
+        // P.V of tile j-1 is complete (S_t(j) was issued after it): rescale
+        // the O rows in TMEM. The accesses are warp-wide, so the whole warp
+        // takes the new maxima.
         const float m_new = fmaxf(m, mxs);
         const float alpha = fast_exp2(m - m_new);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t o[64];
-          tmem_ld32(tO + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-          tmem_ld32(tO + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+        // 32 columns at a time: all of S is held in registers meanwhile
+#pragma unroll 1
+        for (int c = 0; c < kD; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 64; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-          tmem_st32(tO + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + c, o);
         }
         tmem_wait_st();
         l *= alpha;
+        lr *= alpha;
         m = m_new;
       }
 
-      // pass 2: P = 2^(x * scale - m), packed two per column over the first 64
-      // columns of S_t (keys 64hf.. land in columns 32hf.., already read)
-      const float neg_m = -m;
-      float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
-#pragma unroll 1
+      // P = 2^(x * scale - m), packed two per column over the first 64
+      // columns of S_t (all of S is already in registers)
+      const uint64_t nm = f32x2(-m, -m);
+      uint64_t s0 = 0, s1 = 0, r0 = 0, r1 = 0;
+#pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        uint32_t x[64];
-        tmem_ld32(tS + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-        tmem_ld32(tS + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-        tmem_wait_ld();
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int cc = hf * 64 + 2 * c;
-          float p0 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 0]), p.scale_log2, neg_m));
-          float p1 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 1]), p.scale_log2, neg_m));
-          float p2 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 2]), p.scale_log2, neg_m));
-          float p3 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 3]), p.scale_log2, neg_m));
-          if (need_mask) {
-            p0 = cc + 0 < keep ? p0 : 0.f;
-            p1 = cc + 1 < keep ? p1 : 0.f;
-            p2 = cc + 2 < keep ? p2 : 0.f;
-            p3 = cc + 3 < keep ? p3 : 0.f;
-          }
-          r0 += p0;
-          r1 += p1;
-          r2 += p2;
-          r3 += p3;
+        for (int c = 0; c < 32; ++c) {
+          const int k = hf * 64 + 2 * c;
+          const uint64_t e = fma2(f32x2(__uint_as_float(x[k]), __uint_as_float(x[k + 1])), scl, nm);
+          const float p0 = fast_exp2(f32x2_lo(e)), p1 = fast_exp2(f32x2_hi(e));
           pk[c] = pack_bf16x2(p0, p1);
-          pk[c + 1] = pack_bf16x2(p2, p3);
+          if (c & 1) {
+            add2(s1, f32x2(p0, p1));
+            add2(r1, f32x2(bf16lo(pk[c]), bf16hi(pk[c])));
+          } else {
+            add2(s0, f32x2(p0, p1));
+            add2(r0, f32x2(bf16lo(pk[c]), bf16hi(pk[c])));
+          }
         }
         tmem_st32(tS + hf * 32, pk);
       }
-      l += (r0 + r1) + (r2 + r3);
+      add2(s0, s1);
+      add2(r0, r1);
+      l += f32x2_lo(s0) + f32x2_hi(s0);
+      lr += f32x2_lo(r0) + f32x2_hi(r0);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarP + t));
@@ -421,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n_t > 0 &&
         __all_sync(0xffffffffu, good && wait_(bar(kBarO + t), (n_t - 1) & 1, abort))) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lr;
       const bool store = qi < Lq;
       __nv_bfloat16 *orow =
           p.out + (static_cast<int64_t>(q0 + qi) * p.num_q_heads + head[t]) * kD;
@@ -451,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -485,6 +512,14 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
+  // setmaxnreg.inc waits until registers released by the other warpgroup are
+  // free: launch only a build whose per-thread allocation covers the split
+  static const int launch_regs = [] {
+    cudaFuncAttributes fa{};
+    return cudaFuncGetAttributes(&fa, prefill_kernel) == cudaSuccess ? fa.numRegs : 0;
+  }();
+  if (launch_regs * kThreads < (2 * kSoftmaxRegs + kOtherRegs) * 128)
+    return cudaErrorInvalidConfiguration;
   dim3 grid(p.n_rowtiles, G >= 2 ? a.num_q_heads / 2 : a.num_q_heads, a.num_seqs);
   return launch_pdl(prefill_kernel, grid, dim3(kThreads), kSmemBytes, stream, q_map, k_map, v_map,
                     p);

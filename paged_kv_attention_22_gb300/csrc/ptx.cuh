@@ -276,6 +276,21 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// ---------------------------------------------------------------- registers
+
+// Lower / raise this warpgroup's registers per thread to N (a multiple of 8).
+// Every warp of the warpgroup executes the same one; an increase waits until
+// the registers released by decreases are free, so the shares of all
+// warpgroups must add up to no more than the launch's allocation.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- dependent launch
 
 // Programmatic dependent launch: a kernel launched with programmatic stream
@@ -325,6 +340,25 @@ __device__ __forceinline__ float f32x2_lo(uint64_t v) {
 }
 __device__ __forceinline__ float f32x2_hi(uint64_t v) {
   return __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+
+// max of three fp32 values in one instruction (sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Packed pair d = a * b + c over both halves, each an ordinary fp32 fma.
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// Packed pair acc += b over both halves.
+__device__ __forceinline__ void add2(uint64_t &acc, uint64_t b) {
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(b));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
