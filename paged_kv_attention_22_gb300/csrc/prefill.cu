@@ -51,8 +51,9 @@ constexpr int kKOff = kQOff + kTiles * kTileBytes;
 constexpr int kVOff = kKOff + kStages * kTileBytes;
 constexpr int kBarOff = kVOff + kStages * kTileBytes;
 // barrier slots (8 bytes each)
+// kBarVTail: the last V tile, its rows past the segment's end zeroed
 constexpr int kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKEmpty = 5, kBarVEmpty = 7, kBarS = 9,
-              kBarP = 11, kBarO = 13, kNumBars = 15;
+              kBarP = 11, kBarO = 13, kBarVTail = 15, kNumBars = 16;
 constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
 constexpr int kAbortOff = kTmemSlotOff + 8;
 constexpr int kSmemBytes = kAbortOff + 8 + 1024;  // + slack for 1024-byte alignment
@@ -149,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(bar(kBarQ), 1);
+    mbar_init(bar(kBarVTail), 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(kBarKFull + i), 1);
       mbar_init(bar(kBarVFull + i), 1);
@@ -243,6 +245,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every copy of this CTA is issued: the next kernel may start launching
       if (lane == 0) griddep_launch_dependents();
+      // V rows of the last tile past the segment's last key (poison in a
+      // partly used box, stale data in boxes not loaded) are zeroed once the
+      // tile has landed, so that they never meet a zero probability
+      const int tail_r0 = Lk - (n_max - 1) * kBN;
+      if (good && tail_r0 < kBN) {
+        const int st = (n_max - 1) & 1;
+        good = __all_sync(0xffffffffu, wait_(bar(kBarVFull + st), ((n_max - 1) >> 1) & 1, abort));
+        if (good) {
+          const uint32_t vbase = sV + st * kTileBytes;
+          const int n16 = (kBN - tail_r0) * 16;  // 16-byte pieces over both column halves
+          for (int idx = lane; idx < n16; idx += 32) {
+            const int row = tail_r0 + idx / 16, piece = idx % 16;
+            const uint32_t addr = vbase + (piece / 8) * kHalfBytes + row * 128 + (piece % 8) * 16;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(0u), "r"(0u),
+                         "r"(0u), "r"(0u)
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarVTail));
+        }
+      }
       // wait for the last release of each stage, so that no arrival from the
       // tensor core reaches this CTA's shared memory after it has exited
       for (int j = max(n_max - kStages, 0); good && j < n_max; ++j) {
@@ -251,70 +275,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            wait_(bar(kBarVEmpty + (j & 1)), par, abort));
       }
       if (!good && lane == 0) fail(abort);
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      bool good = __all_sync(0xffffffffu, wait_(bar(kBarQ), 0, abort));
+      // One thread issues every MMA and commit. K, V and Q arrive by TMA (the
+      // barrier's completion orders them before the MMAs); P is written by
+      // other threads' tcgen05.st, so its wait is followed by the tcgen05
+      // fence that pairs with theirs.
+      bool good = wait_(bar(kBarQ), 0, abort);
       int v_ready = -1;  // last KV tile whose V is resident (and tail-zeroed)
       auto issue_s = [&](int t, int j) -> bool {
         const int st = j & 1;
-        if (!__all_sync(0xffffffffu, wait_(bar(kBarKFull + st), (j >> 1) & 1, abort)))
-          return false;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t tS = tmem + t * kBN;
-  #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            mma_bf16_ss(tS, smem_desc_sw128(sQ + t * kTileBytes + off, 16, 1024),
-                        smem_desc_sw128(sK + st * kTileBytes + off, 16, 1024), kIdescQK, kk > 0);
-          }
-          mma_commit(bar(kBarS + t));
+        if (!wait_(bar(kBarKFull + st), (j >> 1) & 1, abort)) return false;
+        const uint32_t tS = tmem + t * kBN;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          mma_bf16_ss(tS, smem_desc_sw128(sQ + t * kTileBytes + off, 16, 1024),
+                      smem_desc_sw128(sK + st * kTileBytes + off, 16, 1024), kIdescQK, kk > 0);
         }
-        __syncwarp();
+        mma_commit(bar(kBarS + t));
         return true;
       };
       auto issue_pv = [&](int t, int j) -> bool {
         const int st = j & 1;
         if (v_ready != j) {
-          if (!__all_sync(0xffffffffu, wait_(bar(kBarVFull + st), (j >> 1) & 1, abort)))
+          const bool tail = Lk - j * kBN < kBN;  // the producer zeroes this tile's tail
+          if (!(tail ? wait_(bar(kBarVTail), 0, abort)
+                     : wait_(bar(kBarVFull + st), (j >> 1) & 1, abort)))
             return false;
-          const int r0 = Lk - j * kBN;  // V rows >= r0 are past the segment's last key
-          if (r0 < kBN) {
-            const uint32_t vbase = sV + st * kTileBytes;
-            const int n16 = (kBN - r0) * 16;  // 16-byte pieces over both column halves
-            for (int idx = lane; idx < n16; idx += 32) {
-              const int row = r0 + idx / 16, piece = idx % 16;
-              const uint32_t addr = vbase + (piece / 8) * kHalfBytes + row * 128 + (piece % 8) * 16;
-              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(0u),
-                           "r"(0u), "r"(0u), "r"(0u)
-                           : "memory");
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
           v_ready = j;
         }
         // P_t(j) is in TMEM once the softmax of tile t has arrived
-        if (!__all_sync(0xffffffffu, wait_(bar(kBarP + t), j & 1, abort))) return false;
+        if (!wait_(bar(kBarP + t), j & 1, abort)) return false;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t tP = tmem + t * kBN;             // P over the first 64 columns of S_t
-          const uint32_t tO = tmem + 2 * kBN + t * kD;
-  #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            mma_bf16_ts(tO, tP + kk * 8,
-                        smem_desc_sw128(sV + st * kTileBytes + kk * 16 * 128, kHalfBytes, 1024),
-                        kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(kBarO + t));
+        const uint32_t tP = tmem + t * kBN;             // P over the first 64 columns of S_t
+        const uint32_t tO = tmem + 2 * kBN + t * kD;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          mma_bf16_ts(tO, tP + kk * 8,
+                      smem_desc_sw128(sV + st * kTileBytes + kk * 16 * 128, kHalfBytes, 1024),
+                      kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        __syncwarp();
+        mma_commit(bar(kBarO + t));
         return true;
       };
       for (int t = 0; good && t < kTiles; ++t)
         if (n_tiles[t] > 0) good = issue_s(t, 0);
-      if (good && lane == 0) mma_commit(bar(kBarKEmpty));  // K(0) is free once those are done
-      __syncwarp();
+      if (good) mma_commit(bar(kBarKEmpty));  // K(0) is free once those are done
       for (int j = 1; good && j <= n_max; ++j) {
         // finish tile j-1 for every query tile, starting tile j where needed
         for (int t = 0; good && t < kTiles; ++t) {
@@ -323,13 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (good && j < n_tiles[t]) good = issue_s(t, j);
         }
         // V(j-1) has had its last P.V; K(j) its last S
-        if (good && lane == 0) {
+        if (good) {
           mma_commit(bar(kBarVEmpty + ((j - 1) & 1)));
           if (j < n_max) mma_commit(bar(kBarKEmpty + (j & 1)));
         }
-        __syncwarp();
       }
-      if (!good && lane == 0) fail(abort);
+      if (!good) fail(abort);
     }
   } else {
     setmaxnreg_inc<kSoftmaxRegs>();
