@@ -371,8 +371,9 @@ def time_e2e(sweep, steps, warmup):
 
 
 def time_prefill(pkv, steps, warmup):
-    """Prefix-cached prefill: store of the 32768 prompt tokens, then prefill."""
-    pre, _ = W.prefix8k()
+    """Prefix-cached prefill: store of the 32768 prompt tokens, then prefill;
+    then the decode step at context 8193 on the same cache."""
+    pre, dec = W.prefix8k()
     kc, vc = _dev(pre.poisoned_pool()), _dev(pre.poisoned_pool())
     pkv.kv_store(_dev(pre.history.k), _dev(pre.history.v), kc, vc, _dev(pre.history.slots))
     st = pre.step
@@ -410,8 +411,43 @@ def time_prefill(pkv, steps, warmup):
     pre_ms = statistics.median(a.elapsed_time(b) for a, b in pre_ev)
     flops = prefill_flops(np.diff(st.cu_seqlens_q), np.diff(st.cu_seqlens_k))
     store_bytes = kv_store_algorithmic_bytes(st.new.num_tokens)
+
+    # decode of one token per sequence at context 8193 over the shared prefix
+    ds = dec.step
+    pkv.kv_store(_dev(ds.new.k), _dev(ds.new.v), kc, vc, _dev(ds.new.slots))
+    dq, dlen = _dev(ds.q), _dev(ds.context_lens)
+    dout = torch.empty_like(dq)
+    dlse = torch.empty((dq.shape[0], dq.shape[1]), dtype=torch.float32, device="cuda")
+    ws = pkv.new_decode_workspace(dq.shape[0], dq.shape[1], W.H_KV, W.HEAD_DIM,
+                                  ds.max_context_len)
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+
+    def dec_once(i=None):
+        if i is not None:
+            dec_ev[i][0].record()
+        pkv.paged_decode_attn(dq, kc, vc, bt, dlen, ds.max_context_len, dec.scale, out=dout,
+                              lse=dlse, workspace=ws)
+        if i is not None:
+            dec_ev[i][1].record()
+
+    for _ in range(max(warmup, 3)):
+        dec_once()
+    torch.cuda.synchronize()
+    for i in range(n):
+        dec_once(i)
+    torch.cuda.synchronize()
+    if pkv.check_device_errors() != 0:
+        raise RuntimeError("device error in the prefix decode leg")
+    dec_ms = statistics.median(a.elapsed_time(b) for a, b in dec_ev)
+    ctx = int(ds.context_lens[0])
+    S = int(ds.context_lens.shape[0])
+    logical = decode_algorithmic_bytes(S, ctx)
+    shared_tokens = 4096  # the cached prefix every sequence attends
+    unique = logical - (S - 1) * shared_tokens * W.H_KV * W.HEAD_DIM * 2 * 2
     return dict(prefill_ms=pre_ms, flops=flops, store_ms=store_ms, store_bytes=store_bytes,
-                launches=2 * n)
+                launches=2 * n, decode_ms=dec_ms, decode_logical_bytes=logical,
+                decode_unique_bytes=unique)
 
 
 # ---------------------------------------------------------------- CPU (oracle) legs
@@ -597,6 +633,15 @@ def main(argv=None):
                    "kv_store_gbs": store_gbs,
                    "kv_store_frac": store_gbs / peaks["hbm_gbs"],
                    "kv_store_tokens": 32768}
+        dsec = pr["decode_ms"] / 1000.0
+        prefill["decode_after_prefix"] = {
+            "workload": "decode of 8 seqs at context 8193 sharing the 4096-token prefix",
+            "us_per_call": pr["decode_ms"] * 1000.0,
+            "logical_gbs": pr["decode_logical_bytes"] / dsec / 1e9,
+            "unique_gbs": pr["decode_unique_bytes"] / dsec / 1e9,
+            "logical_bytes": pr["decode_logical_bytes"],
+            "unique_bytes": pr["decode_unique_bytes"],
+            "frac_unique": pr["decode_unique_bytes"] / dsec / 1e9 / peaks["hbm_gbs"]}
 
     if rank == 0:
         line = {
