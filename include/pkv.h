@@ -64,7 +64,8 @@ typedef enum {
   PKV_ERR_INVALID_ARG = 1,
   PKV_ERR_UNSUPPORTED = 2,
   PKV_ERR_WORKSPACE_TOO_SMALL = 3,
-  PKV_ERR_CUDA = 4
+  PKV_ERR_CUDA = 4,
+  PKV_ERR_OUT_OF_BLOCKS = 5 /* the block manager has too few free blocks (pkv_blocks.h) */
 } pkv_status;
 
 /* Bits of the device error word. */

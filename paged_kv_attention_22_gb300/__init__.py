@@ -29,6 +29,7 @@ PKV_ERR_INVALID_ARG = 1
 PKV_ERR_UNSUPPORTED = 2
 PKV_ERR_WORKSPACE_TOO_SMALL = 3
 PKV_ERR_CUDA = 4
+PKV_ERR_OUT_OF_BLOCKS = 5
 
 DEVERR_SLOT = 0x1
 DEVERR_BLOCK = 0x2
@@ -87,6 +88,27 @@ def lib():
     L.pkv_paged_prefill_attn.restype = ctypes.c_int
     L.pkv_check_device_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     L.pkv_check_device_errors.restype = ctypes.c_int
+    pi32 = ctypes.POINTER(ctypes.c_int32)
+    L.pkv_bm_create.argtypes = [i32, i32]
+    L.pkv_bm_create.restype = P
+    L.pkv_bm_destroy.argtypes = [P]
+    L.pkv_bm_destroy.restype = None
+    L.pkv_bm_num_free_blocks.argtypes = [P]
+    L.pkv_bm_num_free_blocks.restype = i32
+    L.pkv_bm_ref_count.argtypes = [P, i32]
+    L.pkv_bm_ref_count.restype = i32
+    L.pkv_bm_add_sequence.argtypes = [P, i64, P, i32, pi32]
+    L.pkv_bm_add_sequence.restype = ctypes.c_int
+    L.pkv_bm_append_token.argtypes = [P, i64, i32]
+    L.pkv_bm_append_token.restype = ctypes.c_int
+    L.pkv_bm_free_sequence.argtypes = [P, i64]
+    L.pkv_bm_free_sequence.restype = ctypes.c_int
+    L.pkv_bm_num_tokens.argtypes = [P, i64, pi32]
+    L.pkv_bm_num_tokens.restype = ctypes.c_int
+    L.pkv_bm_block_table.argtypes = [P, i64, P, i32, pi32]
+    L.pkv_bm_block_table.restype = ctypes.c_int
+    L.pkv_bm_slots.argtypes = [P, i64, i32, i32, P]
+    L.pkv_bm_slots.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -299,3 +321,79 @@ def check_device_errors(stream=None) -> int:
     _check(lib().pkv_check_device_errors(_stream(stream), ctypes.byref(flags)),
            "pkv_check_device_errors")
     return int(flags.value)
+
+
+class BlockManager:
+    """The host-side KV block manager of libpkv.so (pkv_blocks.h): reference-
+    counted cache blocks with prefix sharing of full blocks; it emits block-table
+    rows and the slots of the tokens to store."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        import numpy as np  # noqa: F401  (used by the methods)
+        self._L = lib()
+        self._h = self._L.pkv_bm_create(int(num_blocks), int(block_size))
+        if not self._h:
+            raise PkvError(PKV_ERR_INVALID_ARG, "pkv_bm_create")
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._L.pkv_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    @property
+    def num_free_blocks(self) -> int:
+        return int(self._L.pkv_bm_num_free_blocks(self._h))
+
+    def ref_count(self, block: int) -> int:
+        return int(self._L.pkv_bm_ref_count(self._h, int(block)))
+
+    def add_sequence(self, seq_id: int, token_ids) -> int:
+        """Admit a prompt; returns how many leading tokens are already cached."""
+        import numpy as np
+        tok = np.ascontiguousarray(token_ids, dtype=np.int32)
+        cached = ctypes.c_int32(0)
+        _check(self._L.pkv_bm_add_sequence(self._h, int(seq_id), tok.ctypes.data, tok.shape[0],
+                                           ctypes.byref(cached)), "pkv_bm_add_sequence")
+        return int(cached.value)
+
+    def append_token(self, seq_id: int, token_id: int) -> None:
+        _check(self._L.pkv_bm_append_token(self._h, int(seq_id), int(token_id)),
+               "pkv_bm_append_token")
+
+    def free_sequence(self, seq_id: int) -> None:
+        _check(self._L.pkv_bm_free_sequence(self._h, int(seq_id)), "pkv_bm_free_sequence")
+
+    def num_tokens(self, seq_id: int) -> int:
+        n = ctypes.c_int32(0)
+        _check(self._L.pkv_bm_num_tokens(self._h, int(seq_id), ctypes.byref(n)),
+               "pkv_bm_num_tokens")
+        return int(n.value)
+
+    def block_table(self, seq_id: int, max_blocks: int = None):
+        """The sequence's block ids, padded with -1 to max_blocks (default: none)."""
+        import numpy as np
+        n = ctypes.c_int32(0)
+        self._L.pkv_bm_block_table(self._h, int(seq_id), None, 0, ctypes.byref(n))
+        width = int(n.value) if max_blocks is None else int(max_blocks)
+        row = np.empty(width, np.int32)
+        _check(self._L.pkv_bm_block_table(self._h, int(seq_id), row.ctypes.data, width,
+                                          ctypes.byref(n)), "pkv_bm_block_table")
+        return row
+
+    def block_tables(self, seq_ids, max_blocks: int):
+        """Block-table rows of several sequences [len(seq_ids), max_blocks]."""
+        import numpy as np
+        return np.stack([self.block_table(s, max_blocks) for s in seq_ids]).astype(np.int32)
+
+    def slots(self, seq_id: int, first: int, count: int):
+        """Cache slots of positions first .. first + count - 1."""
+        import numpy as np
+        out = np.empty(int(count), np.int32)
+        _check(self._L.pkv_bm_slots(self._h, int(seq_id), int(first), int(count),
+                                    out.ctypes.data), "pkv_bm_slots")
+        return out

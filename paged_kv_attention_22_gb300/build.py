@@ -15,7 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libpkv.so")
-SOURCES = ["kv_store.cu", "decode.cu", "prefill.cu", "api.cu", "decode_noalloc.cu"]
+SOURCES = ["kv_store.cu", "decode.cu", "prefill.cu", "api.cu", "decode_noalloc.cu",
+           "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]
@@ -31,7 +32,8 @@ def _needs_rebuild() -> bool:
         return True
     lib_time = os.path.getmtime(LIBRARY)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    deps.append(os.path.join(ROOT, "include", "pkv.h"))
+    include = os.path.join(ROOT, "include")
+    deps += [os.path.join(include, f) for f in os.listdir(include)]
     deps.append(os.path.abspath(__file__))
     return any(os.path.getmtime(d) > lib_time for d in deps)
 

@@ -179,6 +179,7 @@ const char *pkv_status_string(pkv_status status) {
     case PKV_OK: return "PKV_OK";
     case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
     case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    case PKV_ERR_OUT_OF_BLOCKS: return "PKV_ERR_OUT_OF_BLOCKS";
     case PKV_ERR_WORKSPACE_TOO_SMALL: return "PKV_ERR_WORKSPACE_TOO_SMALL";
     case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
   }

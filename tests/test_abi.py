@@ -12,6 +12,8 @@ from paged_kv_attention_22_gb300 import build as pkv_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "pkv.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -21,9 +23,11 @@ def L():
 
 
 def _declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    for path in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+        names.update(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_entry_points():
@@ -51,6 +55,7 @@ def test_error_bits_match_header():
 def test_status_strings(L):
     assert pkv.status_string(0) == "PKV_OK"
     assert pkv.status_string(3) == "PKV_ERR_WORKSPACE_TOO_SMALL"
+    assert pkv.status_string(5) == "PKV_ERR_OUT_OF_BLOCKS"
     assert pkv.status_string(99) == "PKV_ERR_UNKNOWN"
 
 
