@@ -34,11 +34,11 @@ def _load():
     lib.oracle_slot_mapping.argtypes = [P, i32, i32, P, P, i64, i32, P]
     lib.oracle_kv_store.argtypes = [P, P, P, P, P, i64, i64, i64]
     lib.oracle_decode.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32,
-                                  i64, f64, P, P]
+                                  i64, f64, i32, P, P]
     lib.oracle_prefill.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32,
-                                   i32, i64, f64, P, P]
+                                   i32, i64, f64, i32, P, P]
     lib.oracle_attend_rows.argtypes = [P, P, P, P, i64, P, P, P, i32, i32, i32,
-                                       i32, i32, i64, f64, P, P]
+                                       i32, i32, i64, f64, i32, P, P]
     for name in ("oracle_slot_mapping", "oracle_kv_store", "oracle_decode",
                  "oracle_prefill", "oracle_attend_rows"):
         getattr(lib, name).restype = ctypes.c_int
@@ -101,8 +101,9 @@ def kv_store(k, v, k_cache, v_cache, slot_mapping):
                                    _ptr(sm), k.shape[0], row, slots), "kv_store")
 
 
-def decode(q, k_cache, v_cache, block_tables, context_lens, scale):
-    """Decode attention: q [S, H_q, D] -> (out [S, H_q, D], lse [S, H_q]) in float64."""
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale, window=0):
+    """Decode attention: q [S, H_q, D] -> (out [S, H_q, D], lse [S, H_q]) in float64.
+    window > 0: each query sees only the last `window` keys up to itself."""
     q = _c(q, np.uint16)
     bt = _c(block_tables, np.int32)
     cl = _c(context_lens, np.int32)
@@ -113,12 +114,13 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale):
     _check(_load().oracle_decode(_ptr(q), _ptr(_c(k_cache, np.uint16)),
                                  _ptr(_c(v_cache, np.uint16)), _ptr(bt), bt.shape[1],
                                  _ptr(cl), S, H_q, H_kv, D, bs, NB, float(scale),
-                                 _ptr(out), _ptr(lse)), "decode")
+                                 int(window), _ptr(out), _ptr(lse)), "decode")
     return out, lse
 
 
-def prefill(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables, scale):
-    """Varlen causal prefill: q [T_q, H_q, D] -> (out [T_q, H_q, D], lse [T_q, H_q])."""
+def prefill(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables, scale, window=0):
+    """Varlen causal prefill: q [T_q, H_q, D] -> (out [T_q, H_q, D], lse [T_q, H_q]).
+    window > 0: each query sees only the last `window` keys up to itself."""
     q = _c(q, np.uint16)
     cq = _c(cu_seqlens_q, np.int32)
     ck = _c(cu_seqlens_k, np.int32)
@@ -130,15 +132,17 @@ def prefill(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables, scale
     _check(_load().oracle_prefill(_ptr(q), _ptr(_c(k_cache, np.uint16)),
                                   _ptr(_c(v_cache, np.uint16)), _ptr(cq), _ptr(ck),
                                   _ptr(bt), bt.shape[1], cq.shape[0] - 1, H_q, H_kv,
-                                  D, bs, NB, float(scale), _ptr(out), _ptr(lse)),
+                                  D, bs, NB, float(scale), int(window), _ptr(out),
+                                  _ptr(lse)),
            "prefill")
     return out, lse
 
 
 def attend_rows(q_rows, seq_ids, head_ids, n_keys, k_cache, v_cache, block_tables,
-                num_q_heads, scale):
+                num_q_heads, scale, window=0):
     """Attention of sampled rows: row r is query q_rows[r] (head head_ids[r] of
-    sequence seq_ids[r]) over that sequence's first n_keys[r] cached keys."""
+    sequence seq_ids[r]) over that sequence's first n_keys[r] cached keys (the
+    last `window` of them if window > 0)."""
     q_rows = _c(q_rows, np.uint16)
     sid = _c(seq_ids, np.int32)
     hid = _c(head_ids, np.int32)
@@ -152,6 +156,6 @@ def attend_rows(q_rows, seq_ids, head_ids, n_keys, k_cache, v_cache, block_table
                                       _ptr(_c(k_cache, np.uint16)),
                                       _ptr(_c(v_cache, np.uint16)), _ptr(bt),
                                       bt.shape[1], int(num_q_heads), H_kv, D, bs, NB,
-                                      float(scale), _ptr(out), _ptr(lse)),
+                                      float(scale), int(window), _ptr(out), _ptr(lse)),
            "attend_rows")
     return out, lse

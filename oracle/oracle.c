@@ -28,6 +28,12 @@
  * with decode attending to every key p < context_len and prefill query i of a
  * segment (Lq new tokens at the end of Lk keys) attending to p <= Lk - Lq + i.
  *
+ * Sliding window. The serving target of the nano-vllm-sansho README ("Sansho
+ * Fork") is an SWA-256 export: sliding-window attention with a window of 256.
+ * The page does not spell the mask out; the reading taken is the plain one: a
+ * query at position i attends to the last `window` positions up to itself,
+ * keys p with i - window < p <= i (window 0: no window).
+ *
  * Readings where the pages are silent (layout [num_blocks, block_size, H_kv,
  * D] row-major; q head h uses KV head h / (H_q / H_kv); -1 marks both a
  * skipped slot and an unused block-table entry; bottom-right causal alignment
@@ -138,17 +144,24 @@ static int64_t gather_row(const cache_view *c, int32_t s, int64_t p) {
   return block * c->block_size + p % c->block_size;
 }
 
+/* First key a query sees when its keys end at n_keys (the query sits at
+ * position n_keys - 1): 0, or the start of its window. */
+static int64_t window_start(int64_t n_keys, int32_t window) {
+  if (window <= 0 || n_keys <= window) return 0;
+  return n_keys - window;
+}
+
 /*
- * One query row (query head h of sequence s) against logical keys [0, n_keys).
- * z holds n_keys doubles of scratch. Returns ORACLE_BAD_BLOCK if a needed
- * table entry is outside the pool.
+ * One query row (query head h of sequence s) against logical keys
+ * [first, n_keys). z holds n_keys doubles of scratch (indexed by key). Returns
+ * ORACLE_BAD_BLOCK if a needed table entry is outside the pool.
  */
 static int attend_row(const cache_view *c, const uint16_t *q_row, int32_t s,
-                      int32_t h, int64_t n_keys, double scale, double *z,
+                      int32_t h, int64_t first, int64_t n_keys, double scale, double *z,
                       double *out_row, double *lse_out) {
   const int32_t g = h / (c->H_q / c->H_kv);
   const int32_t D = c->D;
-  for (int64_t p = 0; p < n_keys; ++p) {
+  for (int64_t p = first; p < n_keys; ++p) {
     int64_t row = gather_row(c, s, p);
     if (row < 0) return ORACLE_BAD_BLOCK;
     const uint16_t *k_row = c->k_cache + (row * c->H_kv + g) * D;
@@ -157,15 +170,15 @@ static int attend_row(const cache_view *c, const uint16_t *q_row, int32_t s,
     z[p] = scale * dot;
   }
   double M = -INFINITY;
-  for (int64_t p = 0; p < n_keys; ++p)
+  for (int64_t p = first; p < n_keys; ++p)
     if (z[p] > M) M = z[p];
   double L = 0.0;
-  for (int64_t p = 0; p < n_keys; ++p) {
+  for (int64_t p = first; p < n_keys; ++p) {
     z[p] = exp(z[p] - M); /* z now holds the unnormalised weights */
     L += z[p];
   }
   for (int32_t d = 0; d < D; ++d) out_row[d] = 0.0;
-  for (int64_t p = 0; p < n_keys; ++p) {
+  for (int64_t p = first; p < n_keys; ++p) {
     int64_t row = gather_row(c, s, p);
     const uint16_t *v_row = c->v_cache + (row * c->H_kv + g) * D;
     for (int32_t d = 0; d < D; ++d) out_row[d] += z[p] * bf16_to_f64(v_row[d]);
@@ -182,7 +195,8 @@ static int check_heads(int32_t H_q, int32_t H_kv, int32_t D, int32_t bs) {
 
 /*
  * Decode: one query token per sequence, attending to every cached key
- * p < context_lens[s] (the query's own K/V are already stored at p = ctx - 1).
+ * p < context_lens[s] (the query's own K/V are already stored at p = ctx - 1),
+ * or to the last `window` of them.
  * q [S, H_q, D] bf16; out [S, H_q, D] f64; lse [S, H_q] f64.
  */
 int oracle_decode(const uint16_t *q, const uint16_t *k_cache,
@@ -190,8 +204,8 @@ int oracle_decode(const uint16_t *q, const uint16_t *k_cache,
                   int32_t max_blocks, const int32_t *context_lens,
                   int32_t num_seqs, int32_t H_q, int32_t H_kv, int32_t D,
                   int32_t block_size, int64_t num_blocks, double scale,
-                  double *out, double *lse) {
-  if (!check_heads(H_q, H_kv, D, block_size)) return ORACLE_BAD_ARG;
+                  int32_t window, double *out, double *lse) {
+  if (!check_heads(H_q, H_kv, D, block_size) || window < 0) return ORACLE_BAD_ARG;
   int64_t max_ctx = 0;
   for (int32_t s = 0; s < num_seqs; ++s) {
     if (context_lens[s] <= 0) return ORACLE_BAD_ARG;
@@ -212,8 +226,8 @@ int oracle_decode(const uint16_t *q, const uint16_t *k_cache,
     for (int64_t r = 0; r < rows; ++r) {
       if (!z) continue;
       int32_t s = (int32_t)(r / H_q), h = (int32_t)(r % H_q);
-      int rc = attend_row(&c, q + r * D, s, h, context_lens[s], scale, z,
-                          out + r * D, lse + r);
+      int rc = attend_row(&c, q + r * D, s, h, window_start(context_lens[s], window),
+                          context_lens[s], scale, z, out + r * D, lse + r);
       if (rc != ORACLE_OK) {
 #pragma omp critical
         status = rc;
@@ -228,8 +242,9 @@ int oracle_decode(const uint16_t *q, const uint16_t *k_cache,
  * Prefill over a paged cache. Segment s owns query tokens
  * [cu_seqlens_q[s], cu_seqlens_q[s+1]) and keys [0, Lk) with
  * Lk = cu_seqlens_k[s+1] - cu_seqlens_k[s]; its Lq queries are the last Lq
- * positions of the Lk, so query i attends to keys p <= Lk - Lq + i. Keys are
- * always read from the cache (the caller stored them first).
+ * positions of the Lk, so query i attends to keys p <= Lk - Lq + i (with a
+ * window, only the last `window` of those). Keys are always read from the
+ * cache (the caller stored them first).
  * q [T_q, H_q, D] bf16; out [T_q, H_q, D] f64; lse [T_q, H_q] f64.
  */
 int oracle_prefill(const uint16_t *q, const uint16_t *k_cache,
@@ -237,8 +252,9 @@ int oracle_prefill(const uint16_t *q, const uint16_t *k_cache,
                    const int32_t *cu_seqlens_k, const int32_t *block_tables,
                    int32_t max_blocks, int32_t num_seqs, int32_t H_q,
                    int32_t H_kv, int32_t D, int32_t block_size,
-                   int64_t num_blocks, double scale, double *out, double *lse) {
-  if (!check_heads(H_q, H_kv, D, block_size)) return ORACLE_BAD_ARG;
+                   int64_t num_blocks, double scale, int32_t window, double *out,
+                   double *lse) {
+  if (!check_heads(H_q, H_kv, D, block_size) || window < 0) return ORACLE_BAD_ARG;
   int64_t max_k = 0;
   for (int32_t s = 0; s < num_seqs; ++s) {
     int64_t Lq = cu_seqlens_q[s + 1] - cu_seqlens_q[s];
@@ -268,8 +284,8 @@ int oracle_prefill(const uint16_t *q, const uint16_t *k_cache,
       int64_t Lk = cu_seqlens_k[s + 1] - cu_seqlens_k[s];
       int64_t i = t - cu_seqlens_q[s];
       int64_t n_keys = Lk - Lq + i + 1;
-      int rc = attend_row(&c, q + (t * H_q + h) * D, s, h, n_keys, scale, z,
-                          out + (t * H_q + h) * D, lse + t * H_q + h);
+      int rc = attend_row(&c, q + (t * H_q + h) * D, s, h, window_start(n_keys, window),
+                          n_keys, scale, z, out + (t * H_q + h) * D, lse + t * H_q + h);
       if (rc != ORACLE_OK) {
 #pragma omp critical
         status = rc;
@@ -283,8 +299,8 @@ int oracle_prefill(const uint16_t *q, const uint16_t *k_cache,
 /*
  * Sampled rows, for checks at full size: attention of the listed
  * (sequence, query head, number of keys) rows, where row r reads query
- * q_rows[r] (D bf16 values). Used to check a few outputs of very large calls
- * one by one.
+ * q_rows[r] (D bf16 values) and sees keys [0, n_keys[r]), or their last
+ * `window`. Used to check a few outputs of very large calls one by one.
  */
 int oracle_attend_rows(const uint16_t *q_rows, const int32_t *seq_ids,
                        const int32_t *head_ids, const int64_t *n_keys,
@@ -292,8 +308,8 @@ int oracle_attend_rows(const uint16_t *q_rows, const int32_t *seq_ids,
                        const uint16_t *v_cache, const int32_t *block_tables,
                        int32_t max_blocks, int32_t H_q, int32_t H_kv, int32_t D,
                        int32_t block_size, int64_t num_blocks, double scale,
-                       double *out, double *lse) {
-  if (!check_heads(H_q, H_kv, D, block_size)) return ORACLE_BAD_ARG;
+                       int32_t window, double *out, double *lse) {
+  if (!check_heads(H_q, H_kv, D, block_size) || window < 0) return ORACLE_BAD_ARG;
   int64_t max_k = 1;
   for (int64_t r = 0; r < num_rows; ++r) {
     if (n_keys[r] <= 0) return ORACLE_BAD_ARG;
@@ -312,8 +328,9 @@ int oracle_attend_rows(const uint16_t *q_rows, const int32_t *seq_ids,
 #pragma omp for schedule(dynamic, 1)
     for (int64_t r = 0; r < num_rows; ++r) {
       if (!z) continue;
-      int rc = attend_row(&c, q_rows + r * D, seq_ids[r], head_ids[r], n_keys[r],
-                          scale, z, out + r * D, lse + r);
+      int rc = attend_row(&c, q_rows + r * D, seq_ids[r], head_ids[r],
+                          window_start(n_keys[r], window), n_keys[r], scale, z,
+                          out + r * D, lse + r);
       if (rc != ORACLE_OK) {
 #pragma omp critical
         status = rc;

@@ -37,10 +37,11 @@ def logical_kv(stores, seq: int, n_keys: int):
     return k, v
 
 
-def sdpa_rows(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, n_keys_per_row):
+def sdpa_rows(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, n_keys_per_row,
+              first_key_per_row=None):
     """Library attention (torch SDPA, fp64) of query rows q_rows [R, H_q, D] over
-    k, v [Lk, H_kv, D] where row r may see keys [0, n_keys_per_row[r]).
-    Returns (out [R, H_q, D], lse [R, H_q])."""
+    k, v [Lk, H_kv, D] where row r may see keys [first_key_per_row[r] (default 0),
+    n_keys_per_row[r]). Returns (out [R, H_q, D], lse [R, H_q])."""
     q = bf16_bits_to_f64(q_rows).permute(1, 0, 2)            # [H_q, R, D]
     kk = bf16_bits_to_f64(k).permute(1, 0, 2)                # [H_kv, Lk, D]
     vv = bf16_bits_to_f64(v).permute(1, 0, 2)
@@ -50,6 +51,9 @@ def sdpa_rows(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, n_
     R, Lk = q.shape[1], kk.shape[1]
     lim = torch.as_tensor(np.asarray(n_keys_per_row), dtype=torch.int64)
     mask = torch.arange(Lk)[None, :] < lim[:, None]           # [R, Lk]
+    if first_key_per_row is not None:
+        lo = torch.as_tensor(np.asarray(first_key_per_row), dtype=torch.int64)
+        mask &= torch.arange(Lk)[None, :] >= lo[:, None]
     out = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, attn_mask=mask, scale=scale)
     logits = torch.matmul(q, kk.transpose(1, 2)) * scale
     logits = logits.masked_fill(~mask, float("-inf"))

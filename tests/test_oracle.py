@@ -229,6 +229,109 @@ def test_decode_equals_last_prefill_row():
     assert np.array_equal(out_d[0], out_p[n - 1]) and np.array_equal(lse_d[0], lse_p[n - 1])
 
 
+# ---------------------------------------------------------------- sliding window
+# (the SWA-256 serving target of the nano-vllm-sansho README, "Sansho Fork";
+# reading: a query at position i sees keys i - window < p <= i)
+
+@pytest.mark.parametrize("window", [1, 37, 256, 700])
+def test_windowed_decode_matches_banded_library_attention(window):
+    case = W.ragged256_decode()
+    kc, vc = _filled_cache(case, [case.step.new])
+    st = case.step
+    out, lse = oracle.decode(st.q, kc, vc, case.block_tables, st.context_lens, case.scale,
+                             window=window)
+    for s in range(case.num_seqs):
+        n = int(st.context_lens[s])
+        k, v = logical_kv(_stores(case), s, n)
+        ref_out, ref_lse = sdpa_rows(st.q[s:s + 1], k, v, case.scale, [n], [max(0, n - window)])
+        np.testing.assert_allclose(out[s], ref_out[0], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[s], ref_lse[0], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("window", [1, 16, 100])
+def test_windowed_prefill_matches_banded_library_attention(window):
+    case = W.prefill_case("prefix-window", 7, q_lens=[12, 0, 30, 19], k_lens=[12, 5, 50, 64],
+                          block_size=16, num_blocks=40, blocks_per_seq=6)
+    kc, vc = _filled_cache(case, [case.step.new])
+    st = case.step
+    out, lse = oracle.prefill(st.q, kc, vc, st.cu_seqlens_q, st.cu_seqlens_k, case.block_tables,
+                              case.scale, window=window)
+    for s in range(case.num_seqs):
+        q0, q1 = int(st.cu_seqlens_q[s]), int(st.cu_seqlens_q[s + 1])
+        Lq, Lk = q1 - q0, int(st.cu_seqlens_k[s + 1] - st.cu_seqlens_k[s])
+        if Lq == 0:
+            continue
+        k, v = logical_kv(_stores(case), s, Lk)
+        hi = [Lk - Lq + i + 1 for i in range(Lq)]
+        lo = [max(0, n - window) for n in hi]
+        ref_out, ref_lse = sdpa_rows(st.q[q0:q1], k, v, case.scale, hi, lo)
+        np.testing.assert_allclose(out[q0:q1], ref_out, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[q0:q1], ref_lse, rtol=0, atol=1e-12)
+
+
+def test_window_covering_every_key_changes_nothing():
+    case = W.ragged256_decode()
+    kc, vc = _filled_cache(case, [case.step.new])
+    st = case.step
+    full = oracle.decode(st.q, kc, vc, case.block_tables, st.context_lens, case.scale)
+    wide = oracle.decode(st.q, kc, vc, case.block_tables, st.context_lens, case.scale,
+                         window=int(st.context_lens.max()))
+    assert np.array_equal(full[0], wide[0]) and np.array_equal(full[1], wide[1])
+    pre = W.ragged256_prefill()
+    kc, vc = _filled_cache(pre, [pre.step.new])
+    ps = pre.step
+    a = oracle.prefill(ps.q, kc, vc, ps.cu_seqlens_q, ps.cu_seqlens_k, pre.block_tables, pre.scale)
+    b = oracle.prefill(ps.q, kc, vc, ps.cu_seqlens_q, ps.cu_seqlens_k, pre.block_tables, pre.scale,
+                       window=ps.max_seqlen_k)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_window_of_one_returns_the_own_value_and_logit():
+    case = W.tiny_decode()
+    kc, vc = _filled_cache(case, [case.step.new])
+    st = case.step
+    out, lse = oracle.decode(st.q, kc, vc, case.block_tables, st.context_lens, case.scale, window=1)
+    G = case.H_q // case.H_kv
+    for s in range(case.num_seqs):
+        n = int(st.context_lens[s])
+        k, v = logical_kv(_stores(case), s, n)
+        for h in range(case.H_q):
+            kk = bf16_bits_to_f64(k[n - 1, h // G]).numpy()
+            vv = bf16_bits_to_f64(v[n - 1, h // G]).numpy()
+            qq = bf16_bits_to_f64(st.q[s, h]).numpy()
+            assert np.array_equal(out[s, h], vv)
+            assert lse[s, h] == pytest.approx(case.scale * float(np.dot(qq, kk)), abs=1e-12)
+
+
+def test_windowed_row_ignores_keys_before_its_window():
+    window, n = 20, 45
+    case = W.prefill_case("win-causal", 11, q_lens=[n], k_lens=[n], block_size=16,
+                          num_blocks=3, blocks_per_seq=3)
+    run = lambda c: oracle.prefill(c.step.q, *_filled_cache(c, [c.step.new]),
+                                   c.step.cu_seqlens_q, c.step.cu_seqlens_k, c.block_tables,
+                                   c.scale, window=window)
+    out, lse = run(case)
+    # perturb every key/value before position 10: rows i >= 29 see keys >= 10 only
+    sel = case.step.new.positions < 10
+    case.step.new.k[sel] ^= np.uint16(0x1234)
+    case.step.new.v[sel] ^= np.uint16(0x0F0F)
+    out2, lse2 = run(case)
+    assert np.array_equal(out[29:], out2[29:]) and np.array_equal(lse[29:], lse2[29:])
+    assert not np.array_equal(out[:29], out2[:29])
+
+
+def test_windowed_decode_equals_last_windowed_prefill_row():
+    n, window = 45, 19
+    pre = W.prefill_case("pw", 13, [n], [n], block_size=16, num_blocks=4, blocks_per_seq=3)
+    kc, vc = _filled_cache(pre, [pre.step.new])
+    out_p, lse_p = oracle.prefill(pre.step.q, kc, vc, pre.step.cu_seqlens_q,
+                                  pre.step.cu_seqlens_k, pre.block_tables, pre.scale,
+                                  window=window)
+    out_d, lse_d = oracle.decode(pre.step.q[n - 1:n], kc, vc, pre.block_tables,
+                                 np.array([n], np.int32), pre.scale, window=window)
+    assert np.array_equal(out_d[0], out_p[n - 1]) and np.array_equal(lse_d[0], lse_p[n - 1])
+
+
 def test_attend_rows_matches_full_decode():
     case = W.tiny_decode()
     out, lse = _run_decode(case)
