@@ -261,7 +261,8 @@ class Sweep:
             common = (P(d["q"].data_ptr()), P(d["kc"].data_ptr()), P(d["vc"].data_ptr()),
                       P(d["bt"].data_ptr()), d["bt"].shape[1], P(d["ctx"].data_ptr()),
                       self.max_ctx, self.S, self.H_q, self.H_kv, self.D, self.bs, self.NB,
-                      ctypes.c_float(self.scale), P(d["out"].data_ptr()), P(d["lse"].data_ptr()),
+                      ctypes.c_float(self.scale), 0, P(d["out"].data_ptr()),
+                      P(d["lse"].data_ptr()),
                       P(d["ws"].data_ptr()), d["ws"].numel(), P(stream_handle))
             if fused:
                 out.append([(L.pkv_paged_decode_attn_store,

@@ -138,6 +138,11 @@ size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t 
  *   context_lens   device int32 [num_seqs], each in [1, max_context_len]
  *   max_context_len host int: an upper bound of context_lens (sizes the grid)
  *   scale          the logit scale (usually 1/sqrt(head_dim))
+ *   sliding_window 0: every key; W > 0: only the last W keys up to the
+ *                  query's own, p >= context_lens[s] - W (sliding-window
+ *                  attention: the SWA-256 serving target of the
+ *                  nano-vllm-sansho README, "Sansho Fork"); blocks wholly
+ *                  before the window are not read. Negative: PKV_ERR_INVALID_ARG.
  *   out            device bf16 [num_seqs, num_q_heads, head_dim]
  *   lse            device float32 [num_seqs, num_q_heads], or NULL
  *   workspace      device, >= pkv_decode_workspace_size(...) bytes, 16-byte aligned
@@ -149,8 +154,8 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
                                  const int32_t *context_lens, int32_t max_context_len,
                                  int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t block_size, int64_t num_blocks,
-                                 float scale, void *out, float *lse, void *workspace,
-                                 size_t workspace_bytes, void *stream);
+                                 float scale, int32_t sliding_window, void *out, float *lse,
+                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Fused decode step: the KV store of each sequence's new token and paged decode
@@ -173,8 +178,9 @@ pkv_status pkv_paged_decode_attn_store(const void *k_new, const void *v_new,
                                        const int32_t *context_lens, int32_t max_context_len,
                                        int32_t num_seqs, int32_t num_q_heads,
                                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                                       int64_t num_blocks, float scale, void *out, float *lse,
-                                       void *workspace, size_t workspace_bytes, void *stream);
+                                       int64_t num_blocks, float scale, int32_t sliding_window,
+                                       void *out, float *lse, void *workspace,
+                                       size_t workspace_bytes, void *stream);
 
 /*
  * Tuning knob of the decode launch, process-wide (not thread-safe against
@@ -217,7 +223,8 @@ pkv_status pkv_paged_decode_attn_noalloc(const void *q, const void *k_cache, con
                                          int32_t num_seqs, int32_t num_q_heads,
                                          int32_t num_kv_heads, int32_t head_dim,
                                          int32_t block_size, int64_t num_blocks, float scale,
-                                         void *out, float *lse, void *stream);
+                                         int32_t sliding_window, void *out, float *lse,
+                                         void *stream);
 
 /*
  * Bytes of device workspace that pkv_paged_prefill_attn needs (currently 0 for
@@ -234,7 +241,10 @@ size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t max_seqlen_q);
  * Lq == Lk is plain causal attention, Lq < Lk serves a prompt whose first
  * Lk - Lq tokens are cached). Keys are always read from the cache: store the
  * prompt's new K/V first, on the same stream. Lq == 0 writes nothing.
- * Output and lse as in decode, for every query row.
+ * Output and lse as in decode, for every query row. With sliding_window
+ * W > 0 query i sees only keys Lk - Lq + i - W < p <= Lk - Lq + i (the last W
+ * positions up to its own); KV tiles wholly before a CTA's windows are not
+ * read. Negative: PKV_ERR_INVALID_ARG.
  *   q              device bf16 [total_q, num_q_heads, head_dim]
  *   cu_seqlens_q/k device int32 [num_seqs + 1], non-decreasing, from 0
  *   max_seqlen_q/k host ints: upper bounds of Lq and Lk (size the grid)
@@ -250,8 +260,9 @@ pkv_status pkv_paged_prefill_attn(const void *q, const void *k_cache, const void
                                   int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
                                   int32_t max_seqlen_k, int32_t num_q_heads,
                                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                                  int64_t num_blocks, float scale, void *out, float *lse,
-                                  void *workspace, size_t workspace_bytes, void *stream);
+                                  int64_t num_blocks, float scale, int32_t sliding_window,
+                                  void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                  void *stream);
 
 /*
  * Synchronise `stream`, then return in *flags_out the OR of the device error

@@ -69,13 +69,13 @@ def lib():
     L.pkv_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     L.pkv_decode_workspace_size.restype = sz
     L.pkv_paged_decode_attn.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, i64,
-                                        f32, P, P, P, sz, P]
+                                        f32, i32, P, P, P, sz, P]
     L.pkv_paged_decode_attn.restype = ctypes.c_int
     L.pkv_paged_decode_attn_store.argtypes = [P, P, P, P, P, P, P, i32, P, i32, i32, i32, i32,
-                                              i32, i32, i64, f32, P, P, P, sz, P]
+                                              i32, i32, i64, f32, i32, P, P, P, sz, P]
     L.pkv_paged_decode_attn_store.restype = ctypes.c_int
     L.pkv_paged_decode_attn_noalloc.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32,
-                                                i32, i64, f32, P, P, P]
+                                                i32, i64, f32, i32, P, P, P]
     L.pkv_paged_decode_attn_noalloc.restype = ctypes.c_int
     L.pkv_set_programmatic_launch.argtypes = [i32]
     L.pkv_set_programmatic_launch.restype = None
@@ -84,7 +84,7 @@ def lib():
     L.pkv_prefill_workspace_size.argtypes = [i32, i32]
     L.pkv_prefill_workspace_size.restype = sz
     L.pkv_paged_prefill_attn.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
-                                         i32, i32, i64, f32, P, P, P, sz, P]
+                                         i32, i32, i64, f32, i32, P, P, P, sz, P]
     L.pkv_paged_prefill_attn.restype = ctypes.c_int
     L.pkv_check_device_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     L.pkv_check_device_errors.restype = ctypes.c_int
@@ -190,8 +190,10 @@ def decode_set_config(ctas: int = 0, variant: int = 0) -> None:
 
 
 def paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
-                      out=None, lse=None, workspace=None, stream=None, with_lse=True):
-    """q=1 decode attention through block tables. Returns (out, lse)."""
+                      out=None, lse=None, workspace=None, stream=None, with_lse=True,
+                      sliding_window=0):
+    """q=1 decode attention through block tables (sliding_window > 0: each query
+    sees only the last sliding_window keys up to its own). Returns (out, lse)."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     _need(v_cache, "v_cache", torch.bfloat16, 4)
@@ -212,14 +214,14 @@ def paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, max_conte
     _check(lib().pkv_paged_decode_attn(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
         _ptr(context_lens), int(max_context_len), S, H_q, H_kv, D, bs, NB, float(scale),
-        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)),
-        "pkv_paged_decode_attn")
+        int(sliding_window), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+        _stream(stream)), "pkv_paged_decode_attn")
     return out, lse
 
 
 def paged_decode_attn_store(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
                             context_lens, max_context_len, scale, out=None, lse=None,
-                            workspace=None, stream=None, with_lse=True):
+                            workspace=None, stream=None, with_lse=True, sliding_window=0):
     """Fused decode step: store each sequence's new K/V row (position
     context_lens[s] - 1, slot slot_mapping[s]) and attend. Returns (out, lse)."""
     _need(k_new, "k_new", torch.bfloat16, 3)
@@ -247,8 +249,8 @@ def paged_decode_attn_store(k_new, v_new, slot_mapping, q, k_cache, v_cache, blo
     _check(lib().pkv_paged_decode_attn_store(
         _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(q), _ptr(k_cache), _ptr(v_cache),
         _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), int(max_context_len), S,
-        H_q, H_kv, D, bs, NB, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
-        workspace.numel(), _stream(stream)), "pkv_paged_decode_attn_store")
+        H_q, H_kv, D, bs, NB, float(scale), int(sliding_window), _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel(), _stream(stream)), "pkv_paged_decode_attn_store")
     return out, lse
 
 
@@ -257,7 +259,7 @@ DECODE_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def paged_decode_attn_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_context_len,
-                              scale, out, lse=None, stream=None):
+                              scale, out, lse=None, stream=None, sliding_window=0):
     """Decode attention for callers that cannot allocate device memory: same
     result as paged_decode_attn, with the library's static scratch in place of a
     workspace. `out` (and `lse`, if wanted) must be supplied; nothing is
@@ -275,7 +277,8 @@ def paged_decode_attn_noalloc(q, k_cache, v_cache, block_tables, context_lens, m
     _check(lib().pkv_paged_decode_attn_noalloc(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
         _ptr(context_lens), int(max_context_len), S, H_q, H_kv, D, bs, NB, float(scale),
-        _ptr(out), _ptr(lse), _stream(stream)), "pkv_paged_decode_attn_noalloc")
+        int(sliding_window), _ptr(out), _ptr(lse), _stream(stream)),
+        "pkv_paged_decode_attn_noalloc")
     return out, lse
 
 
@@ -285,8 +288,10 @@ def prefill_workspace_size(num_seqs, max_seqlen_q) -> int:
 
 def paged_prefill_attn(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables,
                        max_seqlen_q, max_seqlen_k, scale, out=None, lse=None, workspace=None,
-                       stream=None, with_lse=True):
-    """Varlen causal prefill over the paged cache (bottom-right aligned). Returns (out, lse)."""
+                       stream=None, with_lse=True, sliding_window=0):
+    """Varlen causal prefill over the paged cache (bottom-right aligned;
+    sliding_window > 0: each query sees only the last sliding_window keys up to
+    its own). Returns (out, lse)."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     _need(v_cache, "v_cache", torch.bfloat16, 4)
@@ -309,8 +314,8 @@ def paged_prefill_attn(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_ta
     _check(lib().pkv_paged_prefill_attn(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
         _ptr(block_tables), block_tables.shape[1], S, T, int(max_seqlen_q), int(max_seqlen_k),
-        H_q, H_kv, D, bs, NB, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
-        workspace.numel() if workspace is not None else 0, _stream(stream)),
+        H_q, H_kv, D, bs, NB, float(scale), int(sliding_window), _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel() if workspace is not None else 0, _stream(stream)),
         "pkv_paged_prefill_attn")
     return out, lse
 

@@ -242,12 +242,14 @@ pkv_status decode_common(const void *k_new, const void *v_new, const int32_t *sl
                          const int32_t *block_tables, int32_t max_blocks_per_seq,
                          const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                         int32_t block_size, int64_t num_blocks, float scale, void *out,
-                         float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+                         int32_t block_size, int64_t num_blocks, float scale,
+                         int32_t sliding_window, void *out, float *lse, void *workspace,
+                         size_t workspace_bytes, void *stream) {
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_tables == nullptr ||
       context_lens == nullptr || out == nullptr)
     return PKV_ERR_INVALID_ARG;
-  if (num_seqs <= 0 || max_context_len <= 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (num_seqs <= 0 || max_context_len <= 0 || !std::isfinite(scale) || sliding_window < 0)
+    return PKV_ERR_INVALID_ARG;
   pkv_status st = check_attention_shape(num_q_heads, num_kv_heads, head_dim, block_size,
                                         num_blocks, max_blocks_per_seq);
   if (st != PKV_OK) return st;
@@ -286,6 +288,7 @@ pkv_status decode_common(const void *k_new, const void *v_new, const int32_t *sl
   a.num_blocks = static_cast<int32_t>(num_blocks);
   a.variant = g_decode_variant.load(std::memory_order_relaxed);
   a.grid = decode_grid_ctas(sms, a.variant);
+  a.window = sliding_window;
   a.scale_log2 = scale * kLog2e;
 
   // one box = 16 token rows of a head group (K, V), the group's q rows, or
@@ -330,12 +333,12 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
                                  const int32_t *context_lens, int32_t max_context_len,
                                  int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t block_size, int64_t num_blocks,
-                                 float scale, void *out, float *lse, void *workspace,
-                                 size_t workspace_bytes, void *stream) {
+                                 float scale, int32_t sliding_window, void *out, float *lse,
+                                 void *workspace, size_t workspace_bytes, void *stream) {
   return decode_common(nullptr, nullptr, nullptr, q, k_cache, v_cache, block_tables,
                        max_blocks_per_seq, context_lens, max_context_len, num_seqs, num_q_heads,
-                       num_kv_heads, head_dim, block_size, num_blocks, scale, out, lse,
-                       workspace, workspace_bytes, stream);
+                       num_kv_heads, head_dim, block_size, num_blocks, scale, sliding_window,
+                       out, lse, workspace, workspace_bytes, stream);
 }
 
 pkv_status pkv_paged_decode_attn_store(const void *k_new, const void *v_new,
@@ -345,13 +348,14 @@ pkv_status pkv_paged_decode_attn_store(const void *k_new, const void *v_new,
                                        const int32_t *context_lens, int32_t max_context_len,
                                        int32_t num_seqs, int32_t num_q_heads,
                                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                                       int64_t num_blocks, float scale, void *out, float *lse,
-                                       void *workspace, size_t workspace_bytes, void *stream) {
+                                       int64_t num_blocks, float scale, int32_t sliding_window,
+                                       void *out, float *lse, void *workspace,
+                                       size_t workspace_bytes, void *stream) {
   if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr) return PKV_ERR_INVALID_ARG;
   return decode_common(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
                        max_blocks_per_seq, context_lens, max_context_len, num_seqs, num_q_heads,
-                       num_kv_heads, head_dim, block_size, num_blocks, scale, out, lse,
-                       workspace, workspace_bytes, stream);
+                       num_kv_heads, head_dim, block_size, num_blocks, scale, sliding_window,
+                       out, lse, workspace, workspace_bytes, stream);
 }
 
 size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t max_seqlen_q) {
@@ -366,14 +370,16 @@ pkv_status pkv_paged_prefill_attn(const void *q, const void *k_cache, const void
                                   int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
                                   int32_t max_seqlen_k, int32_t num_q_heads,
                                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                                  int64_t num_blocks, float scale, void *out, float *lse,
-                                  void *workspace, size_t workspace_bytes, void *stream) {
+                                  int64_t num_blocks, float scale, int32_t sliding_window,
+                                  void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
   (void)workspace;
   (void)workspace_bytes;
   if (k_cache == nullptr || v_cache == nullptr || cu_seqlens_q == nullptr ||
       cu_seqlens_k == nullptr || block_tables == nullptr)
     return PKV_ERR_INVALID_ARG;
-  if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || !std::isfinite(scale))
+  if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
+      !std::isfinite(scale) || sliding_window < 0)
     return PKV_ERR_INVALID_ARG;
   if (max_seqlen_q > max_seqlen_k) return PKV_ERR_INVALID_ARG;
   pkv_status st = check_attention_shape(num_q_heads, num_kv_heads, head_dim, block_size,
@@ -403,6 +409,7 @@ pkv_status pkv_paged_prefill_attn(const void *q, const void *k_cache, const void
   a.head_dim = head_dim;
   a.block_size = block_size;
   a.num_blocks = static_cast<int32_t>(num_blocks);
+  a.window = sliding_window;
   a.scale_log2 = scale * kLog2e;
 
   CUtensorMap qmap, kmap, vmap;

@@ -69,8 +69,19 @@ struct DecodeParams {
       num_blocks;
   int32_t hg;        // KV heads per group (= consumer warps)
   int32_t n_groups;  // num_kv_heads / hg
+  int32_t window;    // sliding window (keys per query, its own included), 0: none
   float scale_log2;
 };
+
+// With a sliding window the query of a sequence with ctx keys (at position
+// ctx - 1) sees keys ctx - window .. ctx - 1. Its unit list starts at the
+// chunk that holds the first of them; keys before that chunk are never read.
+__device__ __forceinline__ int first_chunk(int ctx, int window) {
+  return (window > 0 && ctx > window) ? (ctx - window) / kChunk : 0;
+}
+__device__ __forceinline__ int first_key(int ctx, int window) {
+  return (window > 0 && ctx > window) ? ctx - window : 0;
+}
 
 // Shared memory layout for G query heads per KV head, head groups of up to
 // kMaxHG KV heads and NS stages.
@@ -186,7 +197,7 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
         if (ctx <= 0 || ctx > p.max_context_len || ctx > ctx_cap) {
           if (blockIdx.x == 0) atomicOr(&g_decode_errors, kErrContext);
         } else {
-          n = (ctx + kChunk - 1) / kChunk;
+          n = (ctx + kChunk - 1) / kChunk - first_chunk(ctx, p.window);
         }
       }
       int incl = n;  // inclusive warp scan
@@ -233,10 +244,14 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
       const uint32_t nbox = static_cast<uint32_t>(HG * kRowBytes);
       const uint64_t policy = l2_policy_evict_first();
       Cursor cur = locate(prefix, p.num_seqs, n_groups, u_lo);
-      // block-table entry of the unit at `cur`, read one unit ahead
+      // first key of the unit at `cur` and its block-table entry, read one
+      // unit ahead
+      auto unit_key = [&](const Cursor &c) {
+        return (first_chunk(ctx_of[c.s], p.window) + c.k) * kChunk;
+      };
       auto table_entry = [&](const Cursor &c) {
         return p.block_tables[static_cast<int64_t>(c.s) * p.max_blocks +
-                              (c.k * kChunk) / p.block_size];
+                              unit_key(c) / p.block_size];
       };
       int32_t blk = table_entry(cur);
       for (int i = 0; i < n_mine; ++i) {
@@ -257,7 +272,7 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
         mbar_arrive_expect_tx(bar, (ok ? 2 * box : 0) + (with_q ? qbox : 0) +
                                        (with_new ? 2 * nbox : 0));
         if (ok) {
-          const int32_t row = blk * p.block_size + (cur.k * kChunk) % p.block_size;
+          const int32_t row = blk * p.block_size + unit_key(cur) % p.block_size;
           tma_load_3d_hint(stage, &k_map, bar, 0, cur.hg * HG, row, policy);
           tma_load_3d_hint(stage + L::kKBytes, &v_map, bar, 0, cur.hg * HG, row, policy);
         }
@@ -313,7 +328,7 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
   uint64_t o[G][4];   // the lane's 8 output dims per head, as fp32 pairs
   int seg_first_k = 0;
   bool seg_is_first = true;
-  int ctx = 0;
+  int ctx = 0, chunk0 = 0, key_lo = 0;  // the segment's length, first chunk and first key
 
 #pragma unroll 1
   for (int it = 0; it < n_mine; ++it) {
@@ -327,6 +342,8 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
     }
     if (opens) {
       ctx = ctx_of[cur.s];
+      chunk0 = first_chunk(ctx, p.window);
+      key_lo = first_key(ctx, p.window);
       seg_first_k = cur.k;
       seg_is_first = (it == 0);
       const uint8_t *qs = kst + 2 * L::kKBytes + g * G * kRowBytes;
@@ -344,12 +361,14 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
         for (int i = 0; i < 4; ++i) o[h][i] = 0ull;
       }
     }
-    const int nvalid = min(kChunk, ctx - cur.k * kChunk);
+    const int key0 = (chunk0 + cur.k) * kChunk;   // the unit's first key
+    const int nvalid = min(kChunk, ctx - key0);   // keys >= nvalid are past the context
+    const int nskip = key_lo - key0;              // keys < nskip are before the window
     const bool with_new = fused && cur.k == chunks_of(prefix, cur.s) - 1;
     if (with_new) {
       // the unit holds the sequence's new token (key ctx-1): take its K and V
       // rows from the staged inputs, whatever the cache row held when copied
-      const int r_new = ctx - 1 - cur.k * kChunk;
+      const int r_new = ctx - 1 - key0;
       uint8_t *stg = smem + static_cast<size_t>(st) * L::kStageBytes;
       const uint8_t *na = stg + 2 * L::kKBytes + L::kQBytes;
       const int part = lane & 15;
@@ -390,7 +409,7 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
       float q2[2] = {part[h][0], part[h][1]};
       butterfly_half<2>(q2, (sub & 2) != 0, 2);
       const float full = q2[0] + __shfl_xor_sync(0xffffffffu, q2[0], 1);
-      sc[h] = my_key < nvalid ? full : -INFINITY;
+      sc[h] = (my_key < nvalid && my_key >= nskip) ? full : -INFINITY;
     }
 
     // ---- online softmax over the unit (base 2), with a lazy maximum: the
@@ -526,7 +545,8 @@ __device__ __forceinline__ void build_prefix(const DecodeParams &p, int *prefix,
     int n = 0;
     if (s < p.num_seqs) {
       const int ctx = p.context_lens[s];
-      if (ctx > 0 && ctx <= p.max_context_len && ctx <= ctx_cap) n = (ctx + kChunk - 1) / kChunk;
+      if (ctx > 0 && ctx <= p.max_context_len && ctx <= ctx_cap)
+        n = (ctx + kChunk - 1) / kChunk - first_chunk(ctx, p.window);
     }
     int incl = n;
 #pragma unroll
@@ -723,6 +743,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
   p.num_blocks = a.num_blocks;
   p.hg = decode_group_heads(a.num_kv_heads, decode_variant_group_max(a.variant));
   p.n_groups = a.num_kv_heads / p.hg;
+  p.window = a.window;
   p.scale_log2 = a.scale_log2;
   switch (a.num_q_heads / a.num_kv_heads) {
     case 1: return launch_group<1>(a, k_map, v_map, q_map, kn_map, vn_map, p, stream);

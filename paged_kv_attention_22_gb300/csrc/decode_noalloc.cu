@@ -47,7 +47,8 @@ extern "C" pkv_status pkv_paged_decode_attn_noalloc(
     const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
     int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t max_context_len,
     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-    int32_t block_size, int64_t num_blocks, float scale, void *out, float *lse, void *stream) {
+    int32_t block_size, int64_t num_blocks, float scale, int32_t sliding_window, void *out,
+    float *lse, void *stream) {
   const size_t need =
       pkv_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len);
   if (need == 0) return PKV_ERR_INVALID_ARG;
@@ -59,6 +60,6 @@ extern "C" pkv_status pkv_paged_decode_attn_noalloc(
   // call reads back, it writes first.
   return pkv_paged_decode_attn(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                                max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                               block_size, num_blocks, scale, out, lse, scratch, kScratchBytes,
-                               stream);
+                               block_size, num_blocks, scale, sliding_window, out, lse, scratch,
+                               kScratchBytes, stream);
 }

@@ -79,6 +79,7 @@ struct DecodeArgs {
   int32_t num_blocks;
   int32_t grid;             // CTAs (persistent; one per SM by default)
   int32_t variant;          // launch shape (see kDecodeNumVariants)
+  int32_t window;           // sliding window in keys (0: none)
   float scale_log2;         // scale * log2(e)
 };
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
@@ -97,6 +98,7 @@ struct PrefillArgs {
   int32_t num_seqs, total_q, max_seqlen_q, max_seqlen_k;
   int32_t num_q_heads, num_kv_heads, head_dim, block_size;
   int32_t num_blocks;
+  int32_t window;  // sliding window in keys (0: none)
   float scale_log2;
 };
 cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,

@@ -77,6 +77,7 @@ struct PrefillParams {
   float *lse;
   int32_t max_blocks, num_seqs, total_q, max_seqlen_q, max_seqlen_k;
   int32_t num_q_heads, num_kv_heads, block_size, num_blocks, n_rowtiles;
+  int32_t window;  // sliding window in keys (0: none)
   float scale_log2;
 };
 
@@ -141,6 +142,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int n_max = max(n_tiles[0], n_tiles[1]);
   if (n_max == 0) return;
+  // With a sliding window query i sees keys >= diag + i - window + 1: the KV
+  // tiles before the one that holds the earliest such key of this CTA's rows
+  // are skipped. Steps jj = 0 .. n_steps - 1 cover KV tiles j_start + jj;
+  // stages and barrier phases count steps.
+  int j_start = 0;
+  if (p.window > 0) {
+    int lo = Lk;
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t)
+      if (n_tiles[t] > 0) lo = min(lo, max(0, diag + row0[t] - p.window + 1));
+    j_start = lo / kBN;
+  }
+  const int n_steps = n_max - j_start;
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + kQOff, sK = sbase + kKOff, sV = sbase + kVOff;
@@ -203,10 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t *table = p.block_tables + static_cast<int64_t>(s) * p.max_blocks;
       auto box_key = [&](int j) { return j * kBN + lane * kBoxRows; };
       auto has_box = [&](int j) { return lane < kBoxes && j < n_max && box_key(j) < Lk; };
-      int32_t next_blk = has_box(0) ? __ldg(table + box_key(0) / p.block_size) : -1;
+      int32_t next_blk = has_box(j_start) ? __ldg(table + box_key(j_start) / p.block_size) : -1;
       bool good = true;
-      for (int j = 0; j < n_max; ++j) {
-        const int st = j & 1;
+      for (int jj = 0; jj < n_steps; ++jj) {
+        const int j = j_start + jj;
+        const int st = jj & 1;
         const int32_t blk = next_blk;
         if (has_box(j + 1)) next_blk = __ldg(table + box_key(j + 1) / p.block_size);
         int32_t row = -1;
@@ -218,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t bytes =
             __popc(__ballot_sync(0xffffffffu, row >= 0)) * 2u * kBoxRows * 128u;
-        if (j >= kStages &&
-            !__all_sync(0xffffffffu, wait_(bar(kBarKEmpty + st), ((j >> 1) - 1) & 1, abort))) {
+        if (jj >= kStages &&
+            !__all_sync(0xffffffffu, wait_(bar(kBarKEmpty + st), ((jj >> 1) - 1) & 1, abort))) {
           good = false;
           break;
         }
@@ -230,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(kdst, &k_map, bar(kBarKFull + st), 0, g, row);
           tma_load_3d(kdst + kHalfBytes, &k_map, bar(kBarKFull + st), 64, g, row);
         }
-        if (j >= kStages &&
-            !__all_sync(0xffffffffu, wait_(bar(kBarVEmpty + st), ((j >> 1) - 1) & 1, abort))) {
+        if (jj >= kStages &&
+            !__all_sync(0xffffffffu, wait_(bar(kBarVEmpty + st), ((jj >> 1) - 1) & 1, abort))) {
           good = false;
           break;
         }
@@ -250,8 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tile has landed, so that they never meet a zero probability
       const int tail_r0 = Lk - (n_max - 1) * kBN;
       if (good && tail_r0 < kBN) {
-        const int st = (n_max - 1) & 1;
-        good = __all_sync(0xffffffffu, wait_(bar(kBarVFull + st), ((n_max - 1) >> 1) & 1, abort));
+        const int st = (n_steps - 1) & 1;
+        good = __all_sync(0xffffffffu, wait_(bar(kBarVFull + st), ((n_steps - 1) >> 1) & 1, abort));
         if (good) {
           const uint32_t vbase = sV + st * kTileBytes;
           const int n16 = (kBN - tail_r0) * 16;  // 16-byte pieces over both column halves
@@ -269,10 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // wait for the last release of each stage, so that no arrival from the
       // tensor core reaches this CTA's shared memory after it has exited
-      for (int j = max(n_max - kStages, 0); good && j < n_max; ++j) {
-        const uint32_t par = (j >> 1) & 1;
-        good = __all_sync(0xffffffffu, wait_(bar(kBarKEmpty + (j & 1)), par, abort) &&
-                                           wait_(bar(kBarVEmpty + (j & 1)), par, abort));
+      for (int jj = max(n_steps - kStages, 0); good && jj < n_steps; ++jj) {
+        const uint32_t par = (jj >> 1) & 1;
+        good = __all_sync(0xffffffffu, wait_(bar(kBarKEmpty + (jj & 1)), par, abort) &&
+                                           wait_(bar(kBarVEmpty + (jj & 1)), par, abort));
       }
       if (!good && lane == 0) fail(abort);
     } else if (warp == kMmaWarp && lane == 0) {
@@ -281,11 +296,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // barrier's completion orders them before the MMAs); P is written by
       // other threads' tcgen05.st, so its wait is followed by the tcgen05
       // fence that pairs with theirs.
+      // Steps are counted from the CTA's first KV tile (j_start); a query tile
+      // has steps 0 .. steps_of[t] - 1.
       bool good = wait_(bar(kBarQ), 0, abort);
-      int v_ready = -1;  // last KV tile whose V is resident (and tail-zeroed)
-      auto issue_s = [&](int t, int j) -> bool {
-        const int st = j & 1;
-        if (!wait_(bar(kBarKFull + st), (j >> 1) & 1, abort)) return false;
+      int steps_of[kTiles];
+#pragma unroll
+      for (int t = 0; t < kTiles; ++t) steps_of[t] = n_tiles[t] > 0 ? n_tiles[t] - j_start : 0;
+      int v_ready = -1;  // last step whose V is resident (and tail-zeroed)
+      auto issue_s = [&](int t, int jj) -> bool {
+        const int st = jj & 1;
+        if (!wait_(bar(kBarKFull + st), (jj >> 1) & 1, abort)) return false;
         const uint32_t tS = tmem + t * kBN;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -296,17 +316,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(kBarS + t));
         return true;
       };
-      auto issue_pv = [&](int t, int j) -> bool {
-        const int st = j & 1;
-        if (v_ready != j) {
-          const bool tail = Lk - j * kBN < kBN;  // the producer zeroes this tile's tail
+      auto issue_pv = [&](int t, int jj) -> bool {
+        const int st = jj & 1;
+        if (v_ready != jj) {
+          // the producer zeroes the tail of the segment's last KV tile
+          const bool tail = Lk - (j_start + jj) * kBN < kBN;
           if (!(tail ? wait_(bar(kBarVTail), 0, abort)
-                     : wait_(bar(kBarVFull + st), (j >> 1) & 1, abort)))
+                     : wait_(bar(kBarVFull + st), (jj >> 1) & 1, abort)))
             return false;
-          v_ready = j;
+          v_ready = jj;
         }
-        // P_t(j) is in TMEM once the softmax of tile t has arrived
-        if (!wait_(bar(kBarP + t), j & 1, abort)) return false;
+        // P_t of this step is in TMEM once the softmax of tile t has arrived
+        if (!wait_(bar(kBarP + t), jj & 1, abort)) return false;
         tc_fence_after();
         const uint32_t tP = tmem + t * kBN;             // P over the first 64 columns of S_t
         const uint32_t tO = tmem + 2 * kBN + t * kD;
@@ -314,25 +335,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kBN / 16; ++kk) {
           mma_bf16_ts(tO, tP + kk * 8,
                       smem_desc_sw128(sV + st * kTileBytes + kk * 16 * 128, kHalfBytes, 1024),
-                      kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                      kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar(kBarO + t));
         return true;
       };
       for (int t = 0; good && t < kTiles; ++t)
-        if (n_tiles[t] > 0) good = issue_s(t, 0);
-      if (good) mma_commit(bar(kBarKEmpty));  // K(0) is free once those are done
-      for (int j = 1; good && j <= n_max; ++j) {
-        // finish tile j-1 for every query tile, starting tile j where needed
+        if (steps_of[t] > 0) good = issue_s(t, 0);
+      if (good) mma_commit(bar(kBarKEmpty));  // K of step 0 is free once those are done
+      for (int jj = 1; good && jj <= n_steps; ++jj) {
+        // finish step jj-1 for every query tile, starting step jj where needed
         for (int t = 0; good && t < kTiles; ++t) {
-          if (j - 1 >= n_tiles[t]) continue;
-          good = issue_pv(t, j - 1);
-          if (good && j < n_tiles[t]) good = issue_s(t, j);
+          if (jj - 1 >= steps_of[t]) continue;
+          good = issue_pv(t, jj - 1);
+          if (good && jj < steps_of[t]) good = issue_s(t, jj);
         }
-        // V(j-1) has had its last P.V; K(j) its last S
+        // V of step jj-1 has had its last P.V; K of step jj its last S
         if (good) {
-          mma_commit(bar(kBarVEmpty + ((j - 1) & 1)));
-          if (j < n_max) mma_commit(bar(kBarKEmpty + (j & 1)));
+          mma_commit(bar(kBarVEmpty + ((jj - 1) & 1)));
+          if (jj < n_steps) mma_commit(bar(kBarKEmpty + (jj & 1)));
         }
       }
       if (!good) fail(abort);
@@ -343,12 +364,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp >> 2;                // query tile of this warpgroup
     const int quad = warp & 3;              // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;         // row within the tile == TMEM lane
-    const int n_t = n_tiles[t];
+    const int n_t = n_tiles[t] > 0 ? n_tiles[t] - j_start : 0;  // steps of this tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + t * kBN + lane_off;
     const uint32_t tO = tmem + 2 * kBN + t * kD + lane_off;
     const int qi = row0[t] + r;             // query index within the segment
     const int lim = diag + qi;              // last key this row may see
+    const int first = p.window > 0 ? lim - p.window + 1 : 0;  // first key (may be < 0)
+    // the largest first key of the tile's rows: KV tiles below it need masking
+    const int first_hi = p.window > 0 ? diag + row0[t] + kBM - p.window : 0;
     // Running maximum m (log2 units) and two running sums: l of the fp32
     // probabilities, for the lse, and lr of the same probabilities rounded to
     // bf16 as the P.V product sees them, which normalises the output. The
@@ -358,30 +382,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the sum of the rounded probabilities keeps the output a convex
     // combination of the V rows with the weights the tensor core used, so a
     // large probability rounded to bf16 costs no more than it does under an
-    // exact maximum.
-    float m = -INFINITY, l = 0.f, lr = 0.f;
+    // exact maximum. A row whose first tiles lie wholly before its window
+    // starts from a finite floor, so that its masked logits give probability
+    // 0 and its first visible tile rescales an O of zeros.
+    constexpr float kFloor = -1e30f;
+    float m = kFloor, l = 0.f, lr = 0.f;
     bool good = true;
     const uint64_t scl = f32x2(p.scale_log2, p.scale_log2);
-    for (int j = 0; j < n_t; ++j) {
-      if (!__all_sync(0xffffffffu, wait_(bar(kBarS + t), j & 1, abort))) {
+    for (int jj = 0; jj < n_t; ++jj) {
+      if (!__all_sync(0xffffffffu, wait_(bar(kBarS + t), jj & 1, abort))) {
         good = false;
         break;
       }
       tc_fence_after();
-      const int kbase = j * kBN;
+      const int kbase = (j_start + jj) * kBN;
       uint32_t x[kBN];
 #pragma unroll
       for (int c = 0; c < kBN; c += 32)
         tmem_ld32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(&x[c]));
       tmem_wait_ld();
-      // keys past the row's causal limit or the segment end are masked (their
-      // logit becomes -inf, their probability 0); only the diagonal and the
-      // tail tiles have any
-      if ((kbase + kBN - 1 > diag + row0[t]) || (kbase + kBN > Lk)) {
-        const int keep = min(lim, Lk - 1) - kbase + 1;  // columns < keep are visible
+      // keys past the row's causal limit or the segment end, or before its
+      // window, are masked (their logit becomes -inf, their probability 0);
+      // only the diagonal, the tail and the window's first tiles have any
+      if ((kbase + kBN - 1 > diag + row0[t]) || (kbase + kBN > Lk) || kbase < first_hi) {
+        const int keep = min(lim, Lk - 1) - kbase + 1;  // columns < keep are at or before the limit
+        const int skip = first - kbase;                 // columns < skip are before the window
 #pragma unroll
         for (int c = 0; c < kBN; ++c)
-          if (c >= keep) x[c] = 0xFF800000u;
+          if (c >= keep || c < skip) x[c] = 0xFF800000u;
       }
       // row max of the raw logits (the scale is positive): eight chains of
       // three-input maxima
@@ -396,10 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mx = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
       const float mxs = mx * p.scale_log2;  // -inf stays -inf
 
-      if (j == 0) {
-        m = mxs;  // every row sees key 0, so this is finite
+      if (jj == 0) {
+        m = fmaxf(mxs, kFloor);  // nothing is in O yet
       } else if (__any_sync(0xffffffffu, mxs > m + kLazyMax)) {
-        // P.V of tile j-1 is complete (S_t(j) was issued after it): rescale
+        // P.V of the previous step is complete (this S was issued after it): rescale
         // the O rows in TMEM. The accesses are warp-wide, so the whole warp
         // takes the new maxima.
         const float m_new = fmaxf(m, mxs);
@@ -514,6 +542,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
   p.num_blocks = a.num_blocks;
   const int rows_per_cta = G >= 2 ? kBM : 2 * kBM;
   p.n_rowtiles = (a.max_seqlen_q + rows_per_cta - 1) / rows_per_cta;
+  p.window = a.window;
   p.scale_log2 = a.scale_log2;
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);

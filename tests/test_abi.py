@@ -64,11 +64,12 @@ FAKE = ctypes.c_void_p(0x10000)  # a non-null, 16-byte aligned value never deref
 
 def _decode(L, **kw):
     a = dict(q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, mb=4, cl=FAKE, mcl=64, S=2, Hq=16, Hkv=8, D=128,
-             bs=16, NB=64, scale=0.088, out=FAKE, lse=None, ws=FAKE, wsb=1 << 20)
+             bs=16, NB=64, scale=0.088, win=0, out=FAKE, lse=None, ws=FAKE, wsb=1 << 20)
     a.update(kw)
     return L.pkv_paged_decode_attn(a["q"], a["kc"], a["vc"], a["bt"], a["mb"], a["cl"], a["mcl"],
                                    a["S"], a["Hq"], a["Hkv"], a["D"], a["bs"], a["NB"],
-                                   a["scale"], a["out"], a["lse"], a["ws"], a["wsb"], None)
+                                   a["scale"], a["win"], a["out"], a["lse"], a["ws"], a["wsb"],
+                                   None)
 
 
 def test_decode_argument_checks(L):
@@ -80,6 +81,7 @@ def test_decode_argument_checks(L):
     assert _decode(L, Hq=64, Hkv=8) == pkv.PKV_ERR_UNSUPPORTED
     assert _decode(L, bs=24) == pkv.PKV_ERR_UNSUPPORTED
     assert _decode(L, scale=float("nan")) == pkv.PKV_ERR_INVALID_ARG
+    assert _decode(L, win=-1) == pkv.PKV_ERR_INVALID_ARG
     assert _decode(L, ws=None) == pkv.PKV_ERR_WORKSPACE_TOO_SMALL
     assert _decode(L, S=2048) == pkv.PKV_ERR_UNSUPPORTED
     assert _decode(L, out=ctypes.c_void_p(0x10008)) == pkv.PKV_ERR_INVALID_ARG
@@ -100,15 +102,16 @@ def test_decode_workspace_size(L):
 def test_prefill_argument_checks(L):
     def call(**kw):
         a = dict(q=FAKE, kc=FAKE, vc=FAKE, cq=FAKE, ck=FAKE, bt=FAKE, mb=4, S=2, T=100, mq=64,
-                 mk=64, Hq=16, Hkv=8, D=128, bs=16, NB=64, scale=0.088, out=FAKE)
+                 mk=64, Hq=16, Hkv=8, D=128, bs=16, NB=64, scale=0.088, win=0, out=FAKE)
         a.update(kw)
         return L.pkv_paged_prefill_attn(a["q"], a["kc"], a["vc"], a["cq"], a["ck"], a["bt"],
                                         a["mb"], a["S"], a["T"], a["mq"], a["mk"], a["Hq"],
-                                        a["Hkv"], a["D"], a["bs"], a["NB"], a["scale"], a["out"],
-                                        None, None, 0, None)
+                                        a["Hkv"], a["D"], a["bs"], a["NB"], a["scale"], a["win"],
+                                        a["out"], None, None, 0, None)
     assert call(cq=None) == pkv.PKV_ERR_INVALID_ARG
     assert call(mq=65, mk=64) == pkv.PKV_ERR_INVALID_ARG
     assert call(D=256) == pkv.PKV_ERR_UNSUPPORTED
+    assert call(win=-5) == pkv.PKV_ERR_INVALID_ARG
     assert call(NB=1 << 28, bs=16) == pkv.PKV_ERR_UNSUPPORTED
     # nothing to do: returns OK without touching the device
     assert call(T=0, q=None, out=None) == pkv.PKV_OK

@@ -28,7 +28,7 @@ def _noalloc(L, case, q, kc, vc, bt, ctx, out, lse):
     return L.pkv_paged_decode_attn_noalloc(
         P(q.data_ptr()), P(kc.data_ptr()), P(vc.data_ptr()), P(bt.data_ptr()), bt.shape[1],
         P(ctx.data_ptr()), st.max_context_len, q.shape[0], case.H_q, case.H_kv, case.D,
-        case.block_size, case.num_blocks, ctypes.c_float(case.scale), P(out.data_ptr()),
+        case.block_size, case.num_blocks, ctypes.c_float(case.scale), 0, P(out.data_ptr()),
         P(lse.data_ptr()), P(torch.cuda.current_stream().cuda_stream))
 
 
