@@ -51,13 +51,16 @@ DECODE_CTX = 640
 
 # ---------------------------------------------------------------- arithmetic
 
-def decode_algorithmic_bytes(num_seqs, ctx, H_q=W.H_Q, H_kv=W.H_KV, D=W.HEAD_DIM, bs=256):
+def decode_algorithmic_bytes(num_seqs, ctx, H_q=W.H_Q, H_kv=W.H_KV, D=W.HEAD_DIM, bs=256,
+                             window=0):
     """Bytes a decode call must move at least: K and V rows of the attended
-    tokens, q, out, lse, the used block-table entries and the context length."""
-    kv = ctx * H_kv * D * 2 * 2
+    tokens (the last `window` with a sliding window), q, out, lse, the used
+    block-table entries and the context length."""
+    first = ctx - window if 0 < window < ctx else 0
+    kv = (ctx - first) * H_kv * D * 2 * 2
     q_out = 2 * H_q * D * 2
     lse = H_q * 4
-    table = -(-ctx // bs) * 4
+    table = (-(-ctx // bs) - first // bs) * 4
     return num_seqs * (kv + q_out + lse + table + 4)
 
 
@@ -66,12 +69,17 @@ def kv_store_algorithmic_bytes(num_tokens, H_kv=W.H_KV, D=W.HEAD_DIM):
     return num_tokens * (H_kv * D * 2 * 2 * 2 + 4)
 
 
-def prefill_flops(q_lens, k_lens, H_q=W.H_Q, D=W.HEAD_DIM):
-    """4*D FLOPs per unmasked (query, key, head): Q K^T and P V."""
+def prefill_flops(q_lens, k_lens, H_q=W.H_Q, D=W.HEAD_DIM, window=0):
+    """4*D FLOPs per unmasked (query, key, head): Q K^T and P V. Query i of a
+    segment sees Lk - Lq + i + 1 keys, at most `window` with a sliding window."""
     pairs = 0
     for lq, lk in zip(q_lens, k_lens):
         lq, lk = int(lq), int(lk)
-        pairs += lq * (lk - lq) + lq * (lq + 1) // 2
+        if window <= 0:
+            pairs += lq * (lk - lq) + lq * (lq + 1) // 2
+        else:
+            n = np.arange(lk - lq + 1, lk + 1, dtype=np.int64)  # keys of each query
+            pairs += int(np.minimum(n, window).sum())
     return 4 * D * pairs * H_q
 
 
@@ -222,32 +230,43 @@ def _dev(a):
 class Sweep:
     """The layers' device state and pre-marshalled C-ABI calls."""
 
-    def __init__(self, pkv, seed_base, num_layers=LAYERS):
+    def __init__(self, pkv, seed_base, num_layers=LAYERS, window=0, shard_world=1):
+        """window: sliding window of every decode call (0: none). shard_world > 1:
+        the caches, q and new rows of one rank's KV-head shard only (tensor
+        parallelism over that many ranks; every rank's shard is the same work)."""
+        from paged_kv_attention_22_gb300.shard import head_shard, take_heads
         self.pkv = pkv
         self.L = pkv.lib()
+        self.window = int(window)
         self.layers = []
         self.host_cases = []
         for layer in range(num_layers):
             case = W.sweep64_layer(layer, base_seed=seed_base)
-            kc, vc = _dev(case.poisoned_pool()), _dev(case.poisoned_pool())
-            pkv.kv_store(_dev(case.history.k), _dev(case.history.v), kc, vc,
+            qh, kvh = head_shard(0, shard_world, case.H_q, case.H_kv)
+            hk = lambda a: take_heads(a, kvh, 1)
+            pool = take_heads(case.poisoned_pool(), kvh, 2)
+            kc, vc = _dev(pool), _dev(pool)
+            pkv.kv_store(_dev(hk(case.history.k)), _dev(hk(case.history.v)), kc, vc,
                          _dev(case.history.slots))
             st = case.step
-            S, H_q, D = st.q.shape
-            d = dict(kc=kc, vc=vc, q=_dev(st.q), k=_dev(st.new.k), v=_dev(st.new.v),
+            q = take_heads(st.q, qh, 1)
+            S, H_q, D = q.shape
+            H_kv = pool.shape[2]
+            d = dict(kc=kc, vc=vc, q=_dev(q), k=_dev(hk(st.new.k)), v=_dev(hk(st.new.v)),
                      slots=_dev(st.new.slots), bt=_dev(case.block_tables),
                      ctx=_dev(st.context_lens), out=torch.empty((S, H_q, D), dtype=torch.bfloat16,
                                                                  device="cuda"),
                      lse=torch.empty((S, H_q), dtype=torch.float32, device="cuda"))
-            d["ws"] = pkv.new_decode_workspace(S, H_q, case.H_kv, D, st.max_context_len)
+            d["ws"] = pkv.new_decode_workspace(S, H_q, H_kv, D, st.max_context_len)
             self.layers.append(d)
             self.host_cases.append(case)
         torch.cuda.synchronize()
         if pkv.check_device_errors() != 0:
             raise RuntimeError("device error while filling the caches")
         c0 = self.host_cases[0]
-        self.S, self.H_q, self.D = c0.step.q.shape
-        self.H_kv, self.bs, self.NB = c0.H_kv, c0.block_size, c0.num_blocks
+        self.S, self.H_q, self.D = self.layers[0]["q"].shape
+        self.H_kv = self.layers[0]["kc"].shape[2]
+        self.bs, self.NB = c0.block_size, c0.num_blocks
         self.max_ctx = c0.step.max_context_len
         self.scale = c0.scale
 
@@ -261,7 +280,7 @@ class Sweep:
             common = (P(d["q"].data_ptr()), P(d["kc"].data_ptr()), P(d["vc"].data_ptr()),
                       P(d["bt"].data_ptr()), d["bt"].shape[1], P(d["ctx"].data_ptr()),
                       self.max_ctx, self.S, self.H_q, self.H_kv, self.D, self.bs, self.NB,
-                      ctypes.c_float(self.scale), 0, P(d["out"].data_ptr()),
+                      ctypes.c_float(self.scale), self.window, P(d["out"].data_ptr()),
                       P(d["lse"].data_ptr()),
                       P(d["ws"].data_ptr()), d["ws"].numel(), P(stream_handle))
             if fused:
@@ -371,9 +390,10 @@ def time_e2e(sweep, steps, warmup):
     return start.elapsed_time(end), h2d, d2h
 
 
-def time_prefill(pkv, steps, warmup):
+def time_prefill(pkv, steps, warmup, window=0):
     """Prefix-cached prefill: store of the 32768 prompt tokens, then prefill;
-    then the decode step at context 8193 on the same cache."""
+    then the decode step at context 8193 on the same cache (both with the
+    given sliding window)."""
     pre, dec = W.prefix8k()
     kc, vc = _dev(pre.poisoned_pool()), _dev(pre.poisoned_pool())
     pkv.kv_store(_dev(pre.history.k), _dev(pre.history.v), kc, vc, _dev(pre.history.slots))
@@ -396,7 +416,7 @@ def time_prefill(pkv, steps, warmup):
             store_ev[i][1].record()
             pre_ev[i][0].record()
         pkv.paged_prefill_attn(q, kc, vc, cq, ck, bt, st.max_seqlen_q, st.max_seqlen_k, pre.scale,
-                               out=out, lse=lse)
+                               out=out, lse=lse, sliding_window=window)
         if i is not None:
             pre_ev[i][1].record()
 
@@ -410,7 +430,7 @@ def time_prefill(pkv, steps, warmup):
         raise RuntimeError("device error in the prefill leg")
     store_ms = statistics.median(a.elapsed_time(b) for a, b in store_ev)
     pre_ms = statistics.median(a.elapsed_time(b) for a, b in pre_ev)
-    flops = prefill_flops(np.diff(st.cu_seqlens_q), np.diff(st.cu_seqlens_k))
+    flops = prefill_flops(np.diff(st.cu_seqlens_q), np.diff(st.cu_seqlens_k), window=window)
     store_bytes = kv_store_algorithmic_bytes(st.new.num_tokens)
 
     # decode of one token per sequence at context 8193 over the shared prefix
@@ -428,7 +448,7 @@ def time_prefill(pkv, steps, warmup):
         if i is not None:
             dec_ev[i][0].record()
         pkv.paged_decode_attn(dq, kc, vc, bt, dlen, ds.max_context_len, dec.scale, out=dout,
-                              lse=dlse, workspace=ws)
+                              lse=dlse, workspace=ws, sliding_window=window)
         if i is not None:
             dec_ev[i][1].record()
 
@@ -443,12 +463,46 @@ def time_prefill(pkv, steps, warmup):
     dec_ms = statistics.median(a.elapsed_time(b) for a, b in dec_ev)
     ctx = int(ds.context_lens[0])
     S = int(ds.context_lens.shape[0])
-    logical = decode_algorithmic_bytes(S, ctx)
-    shared_tokens = 4096  # the cached prefix every sequence attends
+    logical = decode_algorithmic_bytes(S, ctx, window=window)
+    # the cached prefix every sequence attends (none of it inside a window that
+    # ends 4097 tokens later)
+    shared_tokens = 4096 if window <= 0 or window > ctx - 4096 else 0
     unique = logical - (S - 1) * shared_tokens * W.H_KV * W.HEAD_DIM * 2 * 2
     return dict(prefill_ms=pre_ms, flops=flops, store_ms=store_ms, store_bytes=store_bytes,
                 launches=2 * n, decode_ms=dec_ms, decode_logical_bytes=logical,
                 decode_unique_bytes=unique)
+
+
+def time_block_manager(pkv, steps=200, seqs=64, prompt=640, shared=512, bs=256):
+    """Host cost of the block manager through the Python API: admitting `seqs`
+    prompts of `prompt` tokens that share their first `shared` tokens, then per
+    decode step one appended token per sequence, its slot and the block-table
+    rows of the batch (what a scheduler asks for each step)."""
+    rng = np.random.default_rng(5)
+    max_blocks = -(-(prompt + steps) // bs)
+    bm = pkv.BlockManager(seqs * max_blocks, bs)
+    head = rng.integers(0, 50000, shared).astype(np.int32)
+    prompts = [np.concatenate([head, rng.integers(0, 50000, prompt - shared).astype(np.int32)])
+               for _ in range(seqs)]
+    t0 = time.perf_counter()
+    cached = [bm.add_sequence(s, prompts[s]) for s in range(seqs)]
+    admit_s = time.perf_counter() - t0
+    toks = rng.integers(0, 50000, (steps, seqs)).astype(np.int32)
+    t0 = time.perf_counter()
+    for k in range(steps):
+        slots = np.empty(seqs, np.int32)
+        for s in range(seqs):
+            bm.append_token(s, int(toks[k, s]))
+            slots[s] = bm.slots(s, prompt + k, 1)[0]
+        bm.block_tables(range(seqs), max_blocks)
+    step_s = (time.perf_counter() - t0) / steps
+    return {"workload": f"{seqs} prompts of {prompt} tokens sharing {shared}, block size {bs}; "
+                        f"then {steps} decode steps (append, slot, block-table rows)",
+            "admit_us_per_prompt": admit_s / seqs * 1e6,
+            "cached_tokens_per_prompt": float(np.mean(cached[1:])),
+            "us_per_decode_step": step_s * 1e6,
+            "blocks_in_use": seqs * max_blocks - bm.num_free_blocks,
+            "path": "python API over the C ABI (pkv_blocks.h)"}
 
 
 # ---------------------------------------------------------------- CPU (oracle) legs
@@ -525,6 +579,51 @@ def reference_arm(args):
 
 # ---------------------------------------------------------------- main
 
+def time_extras(pkv, args, peaks, layers):
+    """The sliding-window (SWA-256) decode sweep and prefix prefill, one rank's
+    decode sweep on a 2-way KV-head shard, and the host block manager."""
+    steps = max(args.steps // 2, 10)
+    out = {}
+    window = 256
+    sw = Sweep(pkv, seed_base=4000, num_layers=layers, window=window)
+    g_ms = time_sweep_graph(sw, steps, args.warmup)
+    units = steps * layers * DECODE_SEQS
+    nbytes = (decode_algorithmic_bytes(DECODE_SEQS, DECODE_CTX, window=window) +
+              kv_store_algorithmic_bytes(DECODE_SEQS))
+    per_layer = g_ms / 1000.0 / (steps * layers)
+    out["window_decode"] = {"workload": f"c=64 ctx-640 decode sweep, {layers} layers, sliding "
+                                        f"window {window} (fused store + decode per layer, graph)",
+                            "value": units / (g_ms / 1000.0), "unit": "seq·layer/s",
+                            "us_per_layer": per_layer * 1e6,
+                            "gbs": nbytes / per_layer / 1e9,
+                            "frac": nbytes / per_layer / 1e9 / peaks["hbm_gbs"]}
+    del sw
+    sh = Sweep(pkv, seed_base=4000, num_layers=layers, shard_world=2)
+    g_ms = time_sweep_graph(sh, steps, args.warmup)
+    per_layer = g_ms / 1000.0 / (steps * layers)
+    nbytes = (decode_algorithmic_bytes(DECODE_SEQS, DECODE_CTX, H_q=8, H_kv=4) +
+              kv_store_algorithmic_bytes(DECODE_SEQS, H_kv=4))
+    out["head_shard_decode"] = {"workload": f"one rank of a 2-way KV-head shard (8 q / 4 kv "
+                                            f"heads) of the c=64 ctx-640 sweep, {layers} layers",
+                                "value_per_rank": units / (g_ms / 1000.0), "unit": "seq·layer/s",
+                                "us_per_layer": per_layer * 1e6,
+                                "gbs": nbytes / per_layer / 1e9,
+                                "frac": nbytes / per_layer / 1e9 / peaks["hbm_gbs"]}
+    del sh
+    torch.cuda.empty_cache()
+    pr = time_prefill(pkv, min(args.steps, 10), args.warmup, window=window)
+    tflops = pr["flops"] / (pr["prefill_ms"] / 1000.0) / 1e12
+    out["window_prefill"] = {"workload": f"prefix8k prefill with sliding window {window}",
+                             "value": tflops, "unit": "TFLOP/s", "ms_per_call": pr["prefill_ms"],
+                             "flops_per_call": pr["flops"],
+                             "frac": tflops / peaks["bf16_tflops"],
+                             "decode_us_per_call": pr["decode_ms"] * 1000.0,
+                             "decode_gbs": pr["decode_logical_bytes"] / (pr["decode_ms"] / 1e3) / 1e9}
+    torch.cuda.empty_cache()
+    out["block_manager"] = time_block_manager(pkv)
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -542,6 +641,8 @@ def main(argv=None):
                     help="decode launch shape (warps per CTA x stages per warp)")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layers per step (28 for the real workload; fewer for profiling)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the sliding-window, head-shard and block-manager legs")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -644,6 +745,10 @@ def main(argv=None):
             "unique_bytes": pr["decode_unique_bytes"],
             "frac_unique": pr["decode_unique_bytes"] / dsec / 1e9 / peaks["hbm_gbs"]}
 
+    extras = None
+    if not args.no_extras and not args.no_sweep and not args.no_prefill:
+        extras = time_extras(pkv, args, peaks, layers=8)
+
     if rank == 0:
         line = {
             "metric": METRIC,
@@ -671,6 +776,7 @@ def main(argv=None):
             "unfused": unfused,
             "roofline": roofline,
             "prefill": prefill,
+            "extras": extras,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,

@@ -85,3 +85,33 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "seq·layer/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_windowed_byte_and_flop_counts():
+    # a window covering the context changes nothing
+    assert bench.decode_algorithmic_bytes(3, 640, window=640) == bench.decode_algorithmic_bytes(3, 640)
+    assert bench.decode_algorithmic_bytes(3, 640, window=5000) == bench.decode_algorithmic_bytes(3, 640)
+    # window 256 of 640 keys: 256 K/V rows, blocks 1 and 2 of the table
+    per_seq = 256 * 8 * 128 * 2 * 2 + 2 * 16 * 128 * 2 + 16 * 4 + 2 * 4 + 4
+    assert bench.decode_algorithmic_bytes(64, 640, window=256) == 64 * per_seq
+    # prefill: brute force over (query, key) pairs of a small ragged batch
+    q_lens, k_lens, window = [5, 0, 9], [12, 3, 9], 4
+    pairs = 0
+    for lq, lk in zip(q_lens, k_lens):
+        for i in range(lq):
+            last = lk - lq + i
+            pairs += sum(1 for p in range(lk) if last - window < p <= last)
+    assert bench.prefill_flops(q_lens, k_lens, window=window) == 4 * W.HEAD_DIM * W.H_Q * pairs
+    assert bench.prefill_flops(q_lens, k_lens, window=100) == bench.prefill_flops(q_lens, k_lens)
+
+
+def test_block_manager_leg_runs_on_the_host():
+    import paged_kv_attention_22_gb300 as pkv
+    from paged_kv_attention_22_gb300 import build as pkv_build
+    pkv_build.build()
+    r = bench.time_block_manager(pkv, steps=20, seqs=8)
+    assert r["cached_tokens_per_prompt"] == 512      # the shared 512 tokens are two full blocks
+    assert r["us_per_decode_step"] > 0 and r["admit_us_per_prompt"] > 0
+    # 2 shared blocks + one own block per sequence (its last 128 prompt tokens and
+    # the 20 appended ones fit in it)
+    assert r["blocks_in_use"] == 2 + 8
