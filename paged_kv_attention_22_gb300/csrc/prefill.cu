@@ -90,6 +90,9 @@ __device__ __forceinline__ void fail(volatile int *abort) {
   atomicOr(&g_prefill_errors, kErrTimeout);
 }
 
+// kWindowed: a sliding window is set (p.window > 0). The kernel without one
+// is a separate instantiation, so that it keeps no window bookkeeping at all.
+template <bool kWindowed>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                    const __grid_constant__ CUtensorMap k_map,
@@ -147,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // are skipped. Steps jj = 0 .. n_steps - 1 cover KV tiles j_start + jj;
   // stages and barrier phases count steps.
   int j_start = 0;
-  if (p.window > 0) {
+  if constexpr (kWindowed) {
     int lo = Lk;
 #pragma unroll
     for (int t = 0; t < kTiles; ++t)
@@ -296,12 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // barrier's completion orders them before the MMAs); P is written by
       // other threads' tcgen05.st, so its wait is followed by the tcgen05
       // fence that pairs with theirs.
-      // Steps are counted from the CTA's first KV tile (j_start); a query tile
-      // has steps 0 .. steps_of[t] - 1.
+      // Steps are counted from the CTA's first KV tile (j_start); query tile t
+      // has steps 0 .. n_tiles[t] - j_start - 1 (none if that is not positive).
       bool good = wait_(bar(kBarQ), 0, abort);
-      int steps_of[kTiles];
-#pragma unroll
-      for (int t = 0; t < kTiles; ++t) steps_of[t] = n_tiles[t] > 0 ? n_tiles[t] - j_start : 0;
       int v_ready = -1;  // last step whose V is resident (and tail-zeroed)
       auto issue_s = [&](int t, int jj) -> bool {
         const int st = jj & 1;
@@ -341,14 +341,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       for (int t = 0; good && t < kTiles; ++t)
-        if (steps_of[t] > 0) good = issue_s(t, 0);
+        if (n_tiles[t] - j_start > 0) good = issue_s(t, 0);
       if (good) mma_commit(bar(kBarKEmpty));  // K of step 0 is free once those are done
       for (int jj = 1; good && jj <= n_steps; ++jj) {
         // finish step jj-1 for every query tile, starting step jj where needed
         for (int t = 0; good && t < kTiles; ++t) {
-          if (jj - 1 >= steps_of[t]) continue;
+          if (jj - 1 >= n_tiles[t] - j_start) continue;
           good = issue_pv(t, jj - 1);
-          if (good && jj < steps_of[t]) good = issue_s(t, jj);
+          if (good && jj < n_tiles[t] - j_start) good = issue_s(t, jj);
         }
         // V of step jj-1 has had its last P.V; K of step jj its last S
         if (good) {
@@ -370,9 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + 2 * kBN + t * kD + lane_off;
     const int qi = row0[t] + r;             // query index within the segment
     const int lim = diag + qi;              // last key this row may see
-    const int first = p.window > 0 ? lim - p.window + 1 : 0;  // first key (may be < 0)
+    const int first = kWindowed ? lim - p.window + 1 : 0;  // first key (may be < 0)
     // the largest first key of the tile's rows: KV tiles below it need masking
-    const int first_hi = p.window > 0 ? diag + row0[t] + kBM - p.window : 0;
+    const int first_hi = kWindowed ? diag + row0[t] + kBM - p.window : 0;
     // Running maximum m (log2 units) and two running sums: l of the fp32
     // probabilities, for the lse, and lr of the same probabilities rounded to
     // bf16 as the P.V product sees them, which normalises the output. The
@@ -404,12 +404,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // keys past the row's causal limit or the segment end, or before its
       // window, are masked (their logit becomes -inf, their probability 0);
       // only the diagonal, the tail and the window's first tiles have any
-      if ((kbase + kBN - 1 > diag + row0[t]) || (kbase + kBN > Lk) || kbase < first_hi) {
+      if ((kbase + kBN - 1 > diag + row0[t]) || (kbase + kBN > Lk) ||
+          (kWindowed && kbase < first_hi)) {
         const int keep = min(lim, Lk - 1) - kbase + 1;  // columns < keep are at or before the limit
-        const int skip = first - kbase;                 // columns < skip are before the window
+        if constexpr (kWindowed) {
+          const int skip = first - kbase;               // columns < skip are before the window
 #pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c >= keep || c < skip) x[c] = 0xFF800000u;
+          for (int c = 0; c < kBN; ++c)
+            if (c >= keep || c < skip) x[c] = 0xFF800000u;
+        } else {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c >= keep) x[c] = 0xFF800000u;
+        }
       }
       // row max of the raw logits (the scale is positive): eight chains of
       // three-input maxima
@@ -425,7 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mxs = mx * p.scale_log2;  // -inf stays -inf
 
       if (jj == 0) {
-        m = fmaxf(mxs, kFloor);  // nothing is in O yet
+        // nothing is in O yet; without a window every row sees key 0
+        m = kWindowed ? fmaxf(mxs, kFloor) : mxs;
       } else if (__any_sync(0xffffffffu, mxs > m + kLazyMax)) {
         // P.V of the previous step is complete (this S was issued after it): rescale
         // the O rows in TMEM. The accesses are warp-wide, so the whole warp
@@ -520,6 +528,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+template <bool kWindowed>
+cudaError_t launch_instance(dim3 grid, const CUtensorMap &q_map, const CUtensorMap &k_map,
+                            const CUtensorMap &v_map, const PrefillParams &p,
+                            cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kWindowed>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  // setmaxnreg.inc waits until registers released by the other warpgroup are
+  // free: launch only a build whose per-thread allocation covers the split
+  static const int launch_regs = [] {
+    cudaFuncAttributes fa{};
+    return cudaFuncGetAttributes(&fa, prefill_kernel<kWindowed>) == cudaSuccess ? fa.numRegs : 0;
+  }();
+  if (launch_regs * kThreads < (2 * kSoftmaxRegs + kOtherRegs) * 128)
+    return cudaErrorInvalidConfiguration;
+  return launch_pdl(prefill_kernel<kWindowed>, grid, dim3(kThreads), kSmemBytes, stream, q_map,
+                    k_map, v_map, p);
+}
+
 cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
                            const CUtensorMap &k_map, const CUtensorMap &v_map,
                            cudaStream_t stream) {
@@ -544,20 +571,9 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
   p.n_rowtiles = (a.max_seqlen_q + rows_per_cta - 1) / rows_per_cta;
   p.window = a.window;
   p.scale_log2 = a.scale_log2;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBytes);
-  if (e != cudaSuccess) return e;
-  // setmaxnreg.inc waits until registers released by the other warpgroup are
-  // free: launch only a build whose per-thread allocation covers the split
-  static const int launch_regs = [] {
-    cudaFuncAttributes fa{};
-    return cudaFuncGetAttributes(&fa, prefill_kernel) == cudaSuccess ? fa.numRegs : 0;
-  }();
-  if (launch_regs * kThreads < (2 * kSoftmaxRegs + kOtherRegs) * 128)
-    return cudaErrorInvalidConfiguration;
   dim3 grid(p.n_rowtiles, G >= 2 ? a.num_q_heads / 2 : a.num_q_heads, a.num_seqs);
-  return launch_pdl(prefill_kernel, grid, dim3(kThreads), kSmemBytes, stream, q_map, k_map, v_map,
-                    p);
+  return p.window > 0 ? launch_instance<true>(grid, q_map, k_map, v_map, p, stream)
+                      : launch_instance<false>(grid, q_map, k_map, v_map, p, stream);
 }
 
 cudaError_t take_prefill_errors(cudaStream_t stream, uint32_t *flags) {
