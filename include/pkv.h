@@ -185,10 +185,11 @@ pkv_status pkv_paged_decode_attn_store(const void *k_new, const void *v_new,
 /*
  * Tuning knob of the decode launch, process-wide (not thread-safe against
  * concurrent launches): ctas = number of persistent CTAs (0 = one per SM, the
- * default); variant = launch shape (0 = default: head groups of up to 8 KV
- * heads, three TMA stages per CTA where they fit in shared memory; 1 = the same
- * with two stages; 2 = head groups of up to 4 KV heads, two stages, two CTAs
- * per SM). Results do not depend on either, beyond rounding.
+ * default); variant = launch shape (0 = default: head groups of 8 KV heads and
+ * three TMA stages per CTA when the KV heads split into groups of 8, else the
+ * shape of variant 2; 1 = head groups of up to 8 KV heads, two stages; 2 =
+ * head groups of up to 4 KV heads, two stages, two CTAs per SM). Results do
+ * not depend on either, beyond rounding.
  * A non-default ctas changes pkv_decode_workspace_size.
  */
 void pkv_decode_set_config(int32_t ctas, int32_t variant);

@@ -286,7 +286,11 @@ pkv_status decode_common(const void *k_new, const void *v_new, const int32_t *sl
   a.head_dim = head_dim;
   a.block_size = block_size;
   a.num_blocks = static_cast<int32_t>(num_blocks);
+  // variant 0 picks the shape from the head count: groups of 8 KV heads, one
+  // CTA per SM, where the heads split into groups of 8; otherwise groups of
+  // up to 4 with two CTAs per SM, which keeps more warps streaming per SM
   a.variant = g_decode_variant.load(std::memory_order_relaxed);
+  if (a.variant == 0 && pkv::decode_group_heads(num_kv_heads, 8) < 8) a.variant = 2;
   a.grid = decode_grid_ctas(sms, a.variant);
   a.window = sliding_window;
   a.scale_log2 = scale * kLog2e;
