@@ -172,6 +172,30 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
   const int HG = p.hg;
   const int n_groups = p.n_groups;
 
+  int *prefix = reinterpret_cast<int *>(smem + L::kPrefixOffset);
+  int *ctx_of = prefix + p.num_seqs + 1;
+  const uint32_t full0 = smem_u32(smem + L::kBarOffset);
+  const uint32_t empty0 = full0 + NS * 8;
+  const bool fused = p.k_new != nullptr;
+  // independent of the inputs, so done while the previous kernel finishes:
+  // barrier initialisation and the tensor-map prefetch
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, HG);
+    }
+    fence_barrier_init();
+  }
+  if (warp == HG && lane == 0) {
+    prefetch_tensormap(&k_map);
+    prefetch_tensormap(&v_map);
+    prefetch_tensormap(&q_map);
+    if (fused) {
+      prefetch_tensormap(&kn_map);
+      prefetch_tensormap(&vn_map);
+    }
+  }
+
   griddep_wait();  // inputs written by the previous kernel are visible from here on
   // a CTA gave up waiting (in this or an earlier launch): skip the work until
   // the error word is read and cleared; decided once per CTA
@@ -181,19 +205,29 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
 
   // ---- chunk prefix over sequences (invalid lengths count as empty) and the
   // context lengths themselves, kept in shared memory
-  int *prefix = reinterpret_cast<int *>(smem + L::kPrefixOffset);
-  int *ctx_of = prefix + p.num_seqs + 1;
-  const uint32_t full0 = smem_u32(smem + L::kBarOffset);
-  const uint32_t empty0 = full0 + NS * 8;
   if (warp == 0) {
+    // every length load in flight at once, then the scan
+    for (int base = 0; base < p.num_seqs; base += 128) {
+      int v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int s = base + 32 * u + lane;
+        v[u] = s < p.num_seqs ? p.context_lens[s] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int s = base + 32 * u + lane;
+        if (s < p.num_seqs) ctx_of[s] = v[u];
+      }
+    }
+    __syncwarp();
     int carry = 0;
     const int64_t ctx_cap = static_cast<int64_t>(p.max_blocks) * p.block_size;
     for (int base = 0; base < p.num_seqs; base += 32) {
       const int s = base + lane;
       int n = 0;
       if (s < p.num_seqs) {
-        const int ctx = p.context_lens[s];
-        ctx_of[s] = ctx;
+        const int ctx = ctx_of[s];
         if (ctx <= 0 || ctx > p.max_context_len || ctx > ctx_cap) {
           if (blockIdx.x == 0) atomicOr(&g_decode_errors, kErrContext);
         } else {
@@ -209,14 +243,7 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
       if (s < p.num_seqs) prefix[s] = carry + incl - n;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) {
-      prefix[p.num_seqs] = carry;
-      for (int i = 0; i < NS; ++i) {
-        mbar_init(full0 + 8 * i, 1);
-        mbar_init(empty0 + 8 * i, HG);
-      }
-      fence_barrier_init();
-    }
+    if (lane == 0) prefix[p.num_seqs] = carry;
   }
   __syncthreads();
 
@@ -228,41 +255,41 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
   const int n_mine = static_cast<int>(u_hi - u_lo);
   const uint32_t stage0 = smem_u32(smem);
 
-  const bool fused = p.k_new != nullptr;
   if (warp == HG) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tensormap(&k_map);
-      prefetch_tensormap(&v_map);
-      prefetch_tensormap(&q_map);
-      if (fused) {
-        prefetch_tensormap(&kn_map);
-        prefetch_tensormap(&vn_map);
+    // The whole warp runs the loop: lane l holds the block-table entry of unit
+    // i0 + l of the current batch of 32 units, and the next batch is loaded
+    // while this one is used, so no copy waits on a table read after the
+    // first; lane 0 issues the copies.
+    const uint32_t box = static_cast<uint32_t>(kChunk * HG * kRowBytes);
+    const uint32_t qbox = static_cast<uint32_t>(HG * G * kRowBytes);
+    const uint32_t nbox = static_cast<uint32_t>(HG * kRowBytes);
+    const uint64_t policy = l2_policy_evict_first();
+    // first key of the unit at `c` (the window, if any, starts its list)
+    auto unit_key = [&](const Cursor &c) {
+      return (first_chunk(ctx_of[c.s], p.window) + c.k) * kChunk;
+    };
+    auto entry_of = [&](int i) -> int32_t {  // table entry of this CTA's unit i, 0 past the end
+      if (i >= n_mine) return 0;
+      const Cursor c = locate(prefix, p.num_seqs, n_groups, u_lo + i);
+      return p.block_tables[static_cast<int64_t>(c.s) * p.max_blocks + unit_key(c) / p.block_size];
+    };
+    int32_t batch = entry_of(lane);
+    int32_t next_batch = entry_of(32 + lane);
+    Cursor cur = locate(prefix, p.num_seqs, n_groups, u_lo);
+    for (int i = 0; i < n_mine; ++i) {
+      if (i > 0 && (i & 31) == 0) {
+        batch = next_batch;
+        next_batch = entry_of(i + 32 + lane);
       }
-      const uint32_t box = static_cast<uint32_t>(kChunk * HG * kRowBytes);
-      const uint32_t qbox = static_cast<uint32_t>(HG * G * kRowBytes);
-      const uint32_t nbox = static_cast<uint32_t>(HG * kRowBytes);
-      const uint64_t policy = l2_policy_evict_first();
-      Cursor cur = locate(prefix, p.num_seqs, n_groups, u_lo);
-      // first key of the unit at `cur` and its block-table entry, read one
-      // unit ahead
-      auto unit_key = [&](const Cursor &c) {
-        return (first_chunk(ctx_of[c.s], p.window) + c.k) * kChunk;
-      };
-      auto table_entry = [&](const Cursor &c) {
-        return p.block_tables[static_cast<int64_t>(c.s) * p.max_blocks +
-                              unit_key(c) / p.block_size];
-      };
-      int32_t blk = table_entry(cur);
-      for (int i = 0; i < n_mine; ++i) {
-        const int st = i % NS;
-        Cursor nxt = cur;
-        advance(nxt, prefix, p.num_seqs, n_groups);
-        const int32_t blk_next = (i + 1 < n_mine) ? table_entry(nxt) : 0;
-        if (i >= NS && !mbar_wait(empty0 + 8 * st, ((i / NS) - 1) & 1, &g_decode_errors)) {
-          atomicOr(&g_decode_errors, kErrTimeout);
-          break;
-        }
+      const int32_t blk = __shfl_sync(0xffffffffu, batch, i & 31);
+      const int st = i % NS;
+      if (i >= NS &&
+          !__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * st, ((i / NS) - 1) & 1, &g_decode_errors))) {
+        if (lane == 0) atomicOr(&g_decode_errors, kErrTimeout);
+        break;
+      }
+      if (lane == 0) {
         const uint32_t stage = stage0 + st * L::kStageBytes;
         const uint32_t bar = full0 + 8 * st;
         const bool with_q = (i == 0) || (cur.k == 0);
@@ -282,12 +309,12 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
           tma_load_3d(na, &kn_map, bar, 0, cur.hg * HG, cur.s);
           tma_load_3d(na + L::kNewBytes, &vn_map, bar, 0, cur.hg * HG, cur.s);
         }
-        cur = nxt;
-        blk = blk_next;
       }
-      // every copy of this CTA is issued: the next kernel may start launching
-      griddep_launch_dependents();
+      __syncwarp();
+      advance(cur, prefix, p.num_seqs, n_groups);
     }
+    // every copy of this CTA is issued: the next kernel may start launching
+    if (lane == 0) griddep_launch_dependents();
     return;
   }
   if (warp == HG + 1) {
