@@ -355,28 +355,48 @@ def time_sweep_graph(sweep, steps, warmup, fused=True):
     return start.elapsed_time(end)
 
 
+def _packed(tensors, device):
+    """One byte buffer holding the given tensors back to back (256-byte aligned
+    parts), and views of it shaped like them."""
+    offs, off = [], 0
+    for t in tensors:
+        offs.append(off)
+        off += -(-(t.numel() * t.element_size()) // 256) * 256
+    buf = torch.empty(off, dtype=torch.uint8, device=device)
+    if device == "cpu":
+        buf = buf.pin_memory()
+    views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+             for o, t in zip(offs, tensors)]
+    return buf, views
+
+
 def time_e2e(sweep, steps, warmup):
-    """Through the Python API with pinned host inputs/outputs: per step, copy
-    every layer's q, new k, new v and slots in, run, copy out and lse back."""
+    """Through the Python API with pinned host buffers: per step, one copy of
+    every layer's q, new k, new v and slots from a packed pinned host buffer to
+    the device, the 28 fused calls on views of it, and one copy of every
+    layer's out and lse back to a packed pinned host buffer."""
     pkv = sweep.pkv
-    hosts = []
-    for d in sweep.layers:
-        hosts.append({k: d[k].cpu().pin_memory() for k in ("q", "k", "v", "slots")})
-    outs = [(torch.empty_like(d["out"], device="cpu").pin_memory(),
-             torch.empty_like(d["lse"], device="cpu").pin_memory()) for d in sweep.layers]
-    staging = [{k: torch.empty_like(d[k]) for k in ("q", "k", "v", "slots")} for d in sweep.layers]
-    h2d = sum(t.numel() * t.element_size() for h in hosts for t in h.values())
-    d2h = sum(o.numel() * o.element_size() + l.numel() * l.element_size() for o, l in outs)
+    names = ("q", "k", "v", "slots")
+    ins = [sweep.layers[i][k] for i in range(len(sweep.layers)) for k in names]
+    host_in, host_views = _packed(ins, "cpu")
+    dev_in, dev_views = _packed(ins, "cuda")
+    for hv, t in zip(host_views, ins):
+        hv.copy_(t.cpu())
+    outs = [t for d in sweep.layers for t in (d["out"], d["lse"])]
+    host_out, _ = _packed(outs, "cpu")
+    dev_out, dev_out_views = _packed(outs, "cuda")
+    nk = len(names)
+    h2d = host_in.numel()
+    d2h = host_out.numel()
 
     def step():
-        for d, h, stg, (ho, hl) in zip(sweep.layers, hosts, staging, outs):
-            for k in ("q", "k", "v", "slots"):
-                stg[k].copy_(h[k], non_blocking=True)
-            pkv.paged_decode_attn_store(stg["k"], stg["v"], stg["slots"], stg["q"], d["kc"],
-                                        d["vc"], d["bt"], d["ctx"], sweep.max_ctx, sweep.scale,
-                                        out=d["out"], lse=d["lse"], workspace=d["ws"])
-            ho.copy_(d["out"], non_blocking=True)
-            hl.copy_(d["lse"], non_blocking=True)
+        dev_in.copy_(host_in, non_blocking=True)
+        for i, d in enumerate(sweep.layers):
+            q, k, v, slots = dev_views[nk * i:nk * (i + 1)]
+            pkv.paged_decode_attn_store(k, v, slots, q, d["kc"], d["vc"], d["bt"], d["ctx"],
+                                        sweep.max_ctx, sweep.scale, out=dev_out_views[2 * i],
+                                        lse=dev_out_views[2 * i + 1], workspace=d["ws"])
+        host_out.copy_(dev_out, non_blocking=True)
 
     for _ in range(warmup):
         step()
@@ -717,7 +737,9 @@ def main(argv=None):
             e_max = max_over_ranks(e_ms / 1000.0, device="cuda")
             e_units = sum_over_ranks(n_e2e * layers * DECODE_SEQS, device="cuda")
             e2e = {"value": e_units / e_max, "unit": "seq·layer/s", "h2d_bytes_per_step": h2d,
-                   "d2h_bytes_per_step": d2h, "path": "python API, pinned host buffers"}
+                   "d2h_bytes_per_step": d2h,
+                   "path": "python API; per step one copy of the packed inputs in, the 28 "
+                           "fused calls, one copy of the packed outputs back (pinned host)"}
         del sweep
         torch.cuda.empty_cache()
 
