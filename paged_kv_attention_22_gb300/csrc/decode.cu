@@ -469,26 +469,34 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
     __syncwarp();
 
     // ---- P.V: half-warp `half` takes keys 2*pp + half, a lane covers 8 dims
+    auto pv_key = [&](int key) {
+      const uint4 vv =
+          *reinterpret_cast<const uint4 *>(vst + key * tok_bytes + g * kRowBytes + vcol * 16);
+      const uint32_t wv[4] = {vv.x, vv.y, vv.z, vv.w};
+      uint64_t pr2[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float pr = prob[h * kChunk + key];
+        pr2[h] = f32x2(pr, pr);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t v0 = wv[i] << 16, v1 = wv[i] & 0xFFFF0000u;
+#pragma unroll
+        for (int h = 0; h < G; ++h) ffma2(o[h][i], pr2[h], v0, v1);
+      }
+    };
+    if (nvalid == kChunk) {
+      // a full unit (almost every one): fully unrolled, so that all its loads
+      // can be issued ahead of the arithmetic
+#pragma unroll
+      for (int pp = 0; pp < kChunk / 2; ++pp) pv_key(2 * pp + half);
+    } else {
 #pragma unroll 4
-    for (int pp = 0; pp < kChunk / 2; ++pp) {
-      const int key = 2 * pp + half;
-      if (2 * pp >= nvalid) break;
-      if (key < nvalid) {
-        const uint4 vv =
-            *reinterpret_cast<const uint4 *>(vst + key * tok_bytes + g * kRowBytes + vcol * 16);
-        const uint32_t wv[4] = {vv.x, vv.y, vv.z, vv.w};
-        uint64_t pr2[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float pr = prob[h * kChunk + key];
-          pr2[h] = f32x2(pr, pr);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t v0 = wv[i] << 16, v1 = wv[i] & 0xFFFF0000u;
-#pragma unroll
-          for (int h = 0; h < G; ++h) ffma2(o[h][i], pr2[h], v0, v1);
-        }
+      for (int pp = 0; pp < kChunk / 2; ++pp) {
+        const int key = 2 * pp + half;
+        if (2 * pp >= nvalid) break;
+        if (key < nvalid) pv_key(key);
       }
     }
     // this warp is done with the stage (and with prob): release it (after its
