@@ -284,9 +284,12 @@ class Sweep:
                       P(d["lse"].data_ptr()),
                       P(d["ws"].data_ptr()), d["ws"].numel(), P(stream_handle))
             if fused:
+                # the caches, tables and lengths of a decode step are set before
+                # it: each call may read them while the previous one finishes
                 out.append([(L.pkv_paged_decode_attn_store,
                              (P(d["k"].data_ptr()), P(d["v"].data_ptr()),
-                              P(d["slots"].data_ptr())) + common)])
+                              P(d["slots"].data_ptr())) + common[:-1] +
+                             (self.pkv.DECODE_STABLE_INPUTS, common[-1]))])
             else:
                 out.append([(L.pkv_kv_store,
                              (P(d["k"].data_ptr()), P(d["v"].data_ptr()), P(d["kc"].data_ptr()),
@@ -412,7 +415,8 @@ def time_e2e(sweep, steps, warmup):
             q, kk, v, slots = in_views[nk * i:nk * (i + 1)]
             pkv.paged_decode_attn_store(kk, v, slots, q, d["kc"], d["vc"], d["bt"], d["ctx"],
                                         sweep.max_ctx, sweep.scale, out=out_views[2 * i],
-                                        lse=out_views[2 * i + 1], workspace=d["ws"])
+                                        lse=out_views[2 * i + 1], workspace=d["ws"],
+                                        stable_inputs=True)
         in_free[b].record(compute)
         out_ready[b].record(compute)
         down.wait_event(out_ready[b])

@@ -170,7 +170,20 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
  * Other arguments, the workspace and the error behaviour are those of
  * pkv_paged_decode_attn; an invalid slot raises PKV_DEVERR_SLOT (not written;
  * the attention still uses the new rows).
+ *   flags          0, or PKV_DECODE_STABLE_INPUTS: the caller guarantees that
+ *                  k_cache and v_cache (except the rows this call stores),
+ *                  block_tables and context_lens are written neither by the
+ *                  kernel enqueued just before this call nor by any earlier one
+ *                  that may still be running (with programmatic dependent
+ *                  launch a kernel of this library lets the next one start
+ *                  before it ends). The call then reads them, and starts
+ *                  streaming K/V, while the previous kernel finishes; q,
+ *                  k_new, v_new and slot_mapping are still read only after it
+ *                  has completed. This holds in a decode step whose tables and
+ *                  lengths are set before the step and whose layers each have
+ *                  their own caches.
  */
+#define PKV_DECODE_STABLE_INPUTS 0x1u
 pkv_status pkv_paged_decode_attn_store(const void *k_new, const void *v_new,
                                        const int32_t *slot_mapping, const void *q,
                                        void *k_cache, void *v_cache,
@@ -180,7 +193,7 @@ pkv_status pkv_paged_decode_attn_store(const void *k_new, const void *v_new,
                                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                        int64_t num_blocks, float scale, int32_t sliding_window,
                                        void *out, float *lse, void *workspace,
-                                       size_t workspace_bytes, void *stream);
+                                       size_t workspace_bytes, uint32_t flags, void *stream);
 
 /*
  * Tuning knob of the decode launch, process-wide (not thread-safe against

@@ -31,6 +31,8 @@ PKV_ERR_WORKSPACE_TOO_SMALL = 3
 PKV_ERR_CUDA = 4
 PKV_ERR_OUT_OF_BLOCKS = 5
 
+DECODE_STABLE_INPUTS = 0x1  # flag of paged_decode_attn_store (PKV_DECODE_STABLE_INPUTS)
+
 DEVERR_SLOT = 0x1
 DEVERR_BLOCK = 0x2
 DEVERR_CONTEXT = 0x4
@@ -72,7 +74,8 @@ def lib():
                                         f32, i32, P, P, P, sz, P]
     L.pkv_paged_decode_attn.restype = ctypes.c_int
     L.pkv_paged_decode_attn_store.argtypes = [P, P, P, P, P, P, P, i32, P, i32, i32, i32, i32,
-                                              i32, i32, i64, f32, i32, P, P, P, sz, P]
+                                              i32, i32, i64, f32, i32, P, P, P, sz,
+                                              ctypes.c_uint32, P]
     L.pkv_paged_decode_attn_store.restype = ctypes.c_int
     L.pkv_paged_decode_attn_noalloc.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32,
                                                 i32, i64, f32, i32, P, P, P]
@@ -221,9 +224,13 @@ def paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, max_conte
 
 def paged_decode_attn_store(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
                             context_lens, max_context_len, scale, out=None, lse=None,
-                            workspace=None, stream=None, with_lse=True, sliding_window=0):
+                            workspace=None, stream=None, with_lse=True, sliding_window=0,
+                            stable_inputs=False):
     """Fused decode step: store each sequence's new K/V row (position
-    context_lens[s] - 1, slot slot_mapping[s]) and attend. Returns (out, lse)."""
+    context_lens[s] - 1, slot slot_mapping[s]) and attend. Returns (out, lse).
+    stable_inputs: the caches (but the new rows), block_tables and context_lens
+    are not written by the kernels still in flight on the stream, so the call
+    may read them before the previous kernel ends (PKV_DECODE_STABLE_INPUTS)."""
     _need(k_new, "k_new", torch.bfloat16, 3)
     _need(v_new, "v_new", torch.bfloat16, 3)
     _need(slot_mapping, "slot_mapping", torch.int32, 1)
@@ -250,7 +257,8 @@ def paged_decode_attn_store(k_new, v_new, slot_mapping, q, k_cache, v_cache, blo
         _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(q), _ptr(k_cache), _ptr(v_cache),
         _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), int(max_context_len), S,
         H_q, H_kv, D, bs, NB, float(scale), int(sliding_window), _ptr(out), _ptr(lse),
-        _ptr(workspace), workspace.numel(), _stream(stream)), "pkv_paged_decode_attn_store")
+        _ptr(workspace), workspace.numel(), DECODE_STABLE_INPUTS if stable_inputs else 0,
+        _stream(stream)), "pkv_paged_decode_attn_store")
     return out, lse
 
 

@@ -244,7 +244,7 @@ pkv_status decode_common(const void *k_new, const void *v_new, const int32_t *sl
                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                          int32_t block_size, int64_t num_blocks, float scale,
                          int32_t sliding_window, void *out, float *lse, void *workspace,
-                         size_t workspace_bytes, void *stream) {
+                         size_t workspace_bytes, uint32_t flags, void *stream) {
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_tables == nullptr ||
       context_lens == nullptr || out == nullptr)
     return PKV_ERR_INVALID_ARG;
@@ -293,6 +293,7 @@ pkv_status decode_common(const void *k_new, const void *v_new, const int32_t *sl
   if (a.variant == 0 && pkv::decode_group_heads(num_kv_heads, 8) < 8) a.variant = 2;
   a.grid = decode_grid_ctas(sms, a.variant);
   a.window = sliding_window;
+  a.stable_inputs = (flags & PKV_DECODE_STABLE_INPUTS) != 0 && pkv::pdl_enabled();
   a.scale_log2 = scale * kLog2e;
 
   // one box = 16 token rows of a head group (K, V), the group's q rows, or
@@ -342,7 +343,7 @@ pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void 
   return decode_common(nullptr, nullptr, nullptr, q, k_cache, v_cache, block_tables,
                        max_blocks_per_seq, context_lens, max_context_len, num_seqs, num_q_heads,
                        num_kv_heads, head_dim, block_size, num_blocks, scale, sliding_window,
-                       out, lse, workspace, workspace_bytes, stream);
+                       out, lse, workspace, workspace_bytes, 0u, stream);
 }
 
 pkv_status pkv_paged_decode_attn_store(const void *k_new, const void *v_new,
@@ -354,12 +355,13 @@ pkv_status pkv_paged_decode_attn_store(const void *k_new, const void *v_new,
                                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                        int64_t num_blocks, float scale, int32_t sliding_window,
                                        void *out, float *lse, void *workspace,
-                                       size_t workspace_bytes, void *stream) {
+                                       size_t workspace_bytes, uint32_t flags, void *stream) {
   if (k_new == nullptr || v_new == nullptr || slot_mapping == nullptr) return PKV_ERR_INVALID_ARG;
+  if ((flags & ~PKV_DECODE_STABLE_INPUTS) != 0) return PKV_ERR_INVALID_ARG;
   return decode_common(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
                        max_blocks_per_seq, context_lens, max_context_len, num_seqs, num_q_heads,
                        num_kv_heads, head_dim, block_size, num_blocks, scale, sliding_window,
-                       out, lse, workspace, workspace_bytes, stream);
+                       out, lse, workspace, workspace_bytes, flags, stream);
 }
 
 size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t max_seqlen_q) {

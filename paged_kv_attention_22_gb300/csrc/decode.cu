@@ -70,6 +70,7 @@ struct DecodeParams {
   int32_t hg;        // KV heads per group (= consumer warps)
   int32_t n_groups;  // num_kv_heads / hg
   int32_t window;    // sliding window (keys per query, its own included), 0: none
+  int32_t stable_inputs;  // caches, tables and lengths may be read before the wait
   float scale_log2;
 };
 
@@ -196,7 +197,11 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
     }
   }
 
-  griddep_wait();  // inputs written by the previous kernel are visible from here on
+  // Inputs written by the previous kernel are visible after griddep_wait. With
+  // stable inputs the context lengths, block tables and caches are not among
+  // them: the scan and the first K/V copies go ahead, and every warp waits
+  // before it reads q or the new rows or writes anything.
+  if (!p.stable_inputs) griddep_wait();
   // a CTA gave up waiting (in this or an earlier launch): skip the work until
   // the error word is read and cleared; decided once per CTA
   if (__syncthreads_or(threadIdx.x == 0 &&
@@ -277,6 +282,47 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
     int32_t batch = entry_of(lane);
     int32_t next_batch = entry_of(32 + lane);
     Cursor cur = locate(prefix, p.num_seqs, n_groups, u_lo);
+    // Copies of unit i into its stage: `arm` sets the stage barrier's byte
+    // count (once), `kv` issues the K and V boxes, `inputs` the q and new rows.
+    auto issue = [&](int i, const Cursor &c, int32_t blk, bool arm, bool kv, bool inputs) {
+      if (lane != 0) return;
+      const int st = i % NS;
+      const uint32_t stage = stage0 + st * L::kStageBytes;
+      const uint32_t bar = full0 + 8 * st;
+      const bool with_q = (i == 0) || (c.k == 0);
+      const bool with_new = fused && c.k == chunks_of(prefix, c.s) - 1;
+      const bool ok = blk >= 0 && blk < p.num_blocks;
+      if (arm) {
+        if (!ok) atomicOr(&g_decode_errors, kErrBlock);
+        mbar_arrive_expect_tx(bar, (ok ? 2 * box : 0) + (with_q ? qbox : 0) +
+                                       (with_new ? 2 * nbox : 0));
+      }
+      if (kv && ok) {
+        const int32_t row = blk * p.block_size + unit_key(c) % p.block_size;
+        tma_load_3d_hint(stage, &k_map, bar, 0, c.hg * HG, row, policy);
+        tma_load_3d_hint(stage + L::kKBytes, &v_map, bar, 0, c.hg * HG, row, policy);
+      }
+      if (inputs) {
+        if (with_q) tma_load_3d(stage + 2 * L::kKBytes, &q_map, bar, 0, c.hg * HG * G, c.s);
+        if (with_new) {
+          const uint32_t na = stage + 2 * L::kKBytes + L::kQBytes;
+          tma_load_3d(na, &kn_map, bar, 0, c.hg * HG, c.s);
+          tma_load_3d(na + L::kNewBytes, &vn_map, bar, 0, c.hg * HG, c.s);
+        }
+      }
+    };
+    // with stable inputs the K/V copies of the first stages go out before the
+    // wait for the previous kernel, their q and new rows after it
+    const int pre = p.stable_inputs ? min(NS, n_mine) : 0;
+    if (p.stable_inputs) {
+      Cursor c = cur;
+      for (int i = 0; i < pre; ++i) {
+        issue(i, c, __shfl_sync(0xffffffffu, batch, i), true, true, false);
+        __syncwarp();
+        advance(c, prefix, p.num_seqs, n_groups);
+      }
+      griddep_wait();
+    }
     for (int i = 0; i < n_mine; ++i) {
       if (i > 0 && (i & 31) == 0) {
         batch = next_batch;
@@ -289,27 +335,7 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
         if (lane == 0) atomicOr(&g_decode_errors, kErrTimeout);
         break;
       }
-      if (lane == 0) {
-        const uint32_t stage = stage0 + st * L::kStageBytes;
-        const uint32_t bar = full0 + 8 * st;
-        const bool with_q = (i == 0) || (cur.k == 0);
-        const bool with_new = fused && cur.k == chunks_of(prefix, cur.s) - 1;
-        const bool ok = blk >= 0 && blk < p.num_blocks;
-        if (!ok) atomicOr(&g_decode_errors, kErrBlock);
-        mbar_arrive_expect_tx(bar, (ok ? 2 * box : 0) + (with_q ? qbox : 0) +
-                                       (with_new ? 2 * nbox : 0));
-        if (ok) {
-          const int32_t row = blk * p.block_size + unit_key(cur) % p.block_size;
-          tma_load_3d_hint(stage, &k_map, bar, 0, cur.hg * HG, row, policy);
-          tma_load_3d_hint(stage + L::kKBytes, &v_map, bar, 0, cur.hg * HG, row, policy);
-        }
-        if (with_q) tma_load_3d(stage + 2 * L::kKBytes, &q_map, bar, 0, cur.hg * HG * G, cur.s);
-        if (with_new) {
-          const uint32_t na = stage + 2 * L::kKBytes + L::kQBytes;
-          tma_load_3d(na, &kn_map, bar, 0, cur.hg * HG, cur.s);
-          tma_load_3d(na + L::kNewBytes, &vn_map, bar, 0, cur.hg * HG, cur.s);
-        }
-      }
+      issue(i, cur, blk, i >= pre, i >= pre, true);
       __syncwarp();
       advance(cur, prefix, p.num_seqs, n_groups);
     }
@@ -321,6 +347,7 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
     // ------------------------------------------------------------ store warp
     // the new tokens' K/V rows go to their cache slots: sequence s is stored by
     // CTA s mod W (nothing in this launch reads those rows from the cache)
+    if (p.stable_inputs) griddep_wait();
     if (fused) {
       const int row_vec = p.num_kv_heads * (kRowBytes / 16);
       const int64_t num_slots = static_cast<int64_t>(p.num_blocks) * p.block_size;
@@ -342,6 +369,7 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
   if (warp > HG + 1) return;
 
   // -------------------------------------------------------------- consumers
+  if (p.stable_inputs) griddep_wait();     // before any output or workspace write
   const int g = warp;                      // KV head within the group
   const int tok_bytes = HG * kRowBytes;    // one token row of the group in a stage
   const int sub = lane & 7, grp = lane >> 3;
@@ -779,6 +807,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
   p.hg = decode_group_heads(a.num_kv_heads, decode_variant_group_max(a.variant));
   p.n_groups = a.num_kv_heads / p.hg;
   p.window = a.window;
+  p.stable_inputs = a.stable_inputs ? 1 : 0;
   p.scale_log2 = a.scale_log2;
   switch (a.num_q_heads / a.num_kv_heads) {
     case 1: return launch_group<1>(a, k_map, v_map, q_map, kn_map, vn_map, p, stream);

@@ -80,6 +80,7 @@ struct DecodeArgs {
   int32_t grid;             // CTAs (persistent; one per SM by default)
   int32_t variant;          // launch shape (see kDecodeNumVariants)
   int32_t window;           // sliding window in keys (0: none)
+  bool stable_inputs;       // caches, tables and lengths may be read before the wait
   float scale_log2;         // scale * log2(e)
 };
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,

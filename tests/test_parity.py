@@ -316,3 +316,50 @@ def test_classic_launch_gives_the_same_results():
         pkv.set_programmatic_launch(True)
     for x, y in zip(a, b):
         assert np.array_equal(x["out"], y["out"]) and np.array_equal(x["lse"], y["lse"])
+
+
+def test_fused_store_with_stable_inputs_over_a_chain_of_layers():
+    """The decode step as the engine runs it: one fused call per layer back to
+    back on one stream, each allowed to read its caches, tables and lengths
+    while the previous call finishes (PKV_DECODE_STABLE_INPUTS). Every layer
+    matches the oracle and every cache byte is as stored."""
+    layers = [W.sweep64_layer(i) for i in range(6)]
+    dev = []
+    for case in layers:
+        kc, vc = gpu_pool(case)
+        gpu_store(case.history, kc, vc)
+        dev.append((kc, vc))
+    torch.cuda.synchronize()
+    ws = pkv.new_decode_workspace(64, 16, 8, 128, 640)  # one workspace shared by every layer
+    outs = []
+    for case, (kc, vc) in zip(layers, dev):
+        st = case.step
+        outs.append(pkv.paged_decode_attn_store(
+            dev_bf16(st.new.k), dev_bf16(st.new.v), dev_i32(st.new.slots), dev_bf16(st.q), kc, vc,
+            dev_i32(case.block_tables), dev_i32(st.context_lens), st.max_context_len, case.scale,
+            workspace=ws, stable_inputs=True))
+    assert pkv.check_device_errors() == 0
+    for case, (kc, vc), (o, l) in zip(layers, dev, outs):
+        ref = oracle_run(case)
+        assert_cache_equal(kc, vc, ref["kc"], ref["vc"])
+        assert_close(o.double().cpu().numpy(), l.double().cpu().numpy(), ref["out"], ref["lse"],
+                     what=case.name + " (stable inputs)")
+
+
+def test_fused_store_rejects_unknown_flags():
+    import ctypes
+    case = W.tiny_decode()
+    st = case.step
+    kc, vc = gpu_pool(case)
+    q = dev_bf16(st.q)
+    out = torch.empty_like(q)
+    ws = pkv.new_decode_workspace(st.q.shape[0], 16, 8, 128, st.max_context_len)
+    k, v, slots = dev_bf16(st.new.k), dev_bf16(st.new.v), dev_i32(st.new.slots)
+    bt, ctx = dev_i32(case.block_tables), dev_i32(st.context_lens)
+    P = ctypes.c_void_p
+    rc = pkv.lib().pkv_paged_decode_attn_store(
+        P(k.data_ptr()), P(v.data_ptr()), P(slots.data_ptr()), P(q.data_ptr()), P(kc.data_ptr()),
+        P(vc.data_ptr()), P(bt.data_ptr()), bt.shape[1], P(ctx.data_ptr()), st.max_context_len,
+        q.shape[0], 16, 8, 128, case.block_size, case.num_blocks, ctypes.c_float(case.scale), 0,
+        P(out.data_ptr()), None, P(ws.data_ptr()), ws.numel(), 0x2, None)
+    assert rc == pkv.PKV_ERR_INVALID_ARG
