@@ -422,9 +422,11 @@ pkv_status pkv_paged_prefill_attn(const void *q, const void *k_cache, const void
   const int64_t rows = num_blocks * block_size;
   if ((st = encode_rows_map(&qmap, q, total_q, num_q_heads, head_dim, 64, 1, 128, true)) != PKV_OK)
     return st;
-  if ((st = encode_rows_map(&kmap, k_cache, rows, num_kv_heads, head_dim, 64, 1, 16, true)) != PKV_OK)
+  a.box_rows = pkv::prefill_box_rows(block_size);
+  const uint32_t box = static_cast<uint32_t>(a.box_rows);
+  if ((st = encode_rows_map(&kmap, k_cache, rows, num_kv_heads, head_dim, 64, 1, box, true)) != PKV_OK)
     return st;
-  if ((st = encode_rows_map(&vmap, v_cache, rows, num_kv_heads, head_dim, 64, 1, 16, true)) != PKV_OK)
+  if ((st = encode_rows_map(&vmap, v_cache, rows, num_kv_heads, head_dim, 64, 1, box, true)) != PKV_OK)
     return st;
   cudaError_t e = pkv::launch_prefill(a, qmap, kmap, vmap, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");

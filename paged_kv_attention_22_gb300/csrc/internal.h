@@ -100,8 +100,17 @@ struct PrefillArgs {
   int32_t num_q_heads, num_kv_heads, head_dim, block_size;
   int32_t num_blocks;
   int32_t window;  // sliding window in keys (0: none)
+  int32_t box_rows;  // rows per K/V TMA box: prefill_box_rows(block_size)
   float scale_log2;
 };
+// Rows per K/V box of the prefill kernel: the largest of 128, 64, 32, 16 that
+// divides the block size, so that a box never crosses a cache block and a
+// 128-key tile takes as few copies as the block size allows.
+inline int32_t prefill_box_rows(int32_t block_size) {
+  int32_t r = 128;
+  while (block_size % r != 0) r >>= 1;
+  return r;
+}
 cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
                            const CUtensorMap &k_map, const CUtensorMap &v_map,
                            cudaStream_t stream);

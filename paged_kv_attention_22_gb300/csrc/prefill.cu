@@ -9,9 +9,12 @@
 // One CTA owns two 128-row query tiles that share every K/V tile: with grouped
 // queries (H_q / H_kv >= 2) the two query heads of a head pair over the same
 // 128 rows; without grouping, two consecutive row tiles of one head. 12 warps:
-//   warp 8     TMA producer: both Q tiles once, then K and V tiles of 128 keys
-//              as eight 16-row boxes each (a box never crosses a cache block),
-//              two stages deep, 128-byte swizzled.
+//   warp 8     TMA producer: both Q tiles once, then K and V tiles of 128 keys,
+//              two stages deep, 128-byte swizzled. A tile is copied as boxes of
+//              the largest of 128, 64, 32, 16 rows that divides the block size
+//              (a box never crosses a cache block): each copy costs the TMA
+//              unit a fixed overhead, so one 128-row box per column half
+//              streams far faster than eight 16-row ones.
 //   warp 9     MMA issuer. TMEM holds S_t (128 fp32 columns) and O_t (128) for
 //              each tile t. Per KV tile j and query tile t: S_t = Q_t K_j^T
 //              (A and B from shared memory), then, once the softmax has
@@ -42,7 +45,6 @@ constexpr int kD = 128;
 constexpr int kBM = 128;                       // query rows per tile
 constexpr int kBN = 128;                       // keys per KV tile
 constexpr int kTiles = 2;                      // query tiles per CTA
-constexpr int kBoxRows = 16;                   // rows per K/V TMA box
 constexpr int kHalfBytes = 128 * 128;          // 128 rows x 64 bf16 (one swizzle column group)
 constexpr int kTileBytes = 2 * kHalfBytes;     // 128 rows x 128 bf16
 constexpr int kStages = 2;
@@ -77,7 +79,8 @@ struct PrefillParams {
   float *lse;
   int32_t max_blocks, num_seqs, total_q, max_seqlen_q, max_seqlen_k;
   int32_t num_q_heads, num_kv_heads, block_size, num_blocks, n_rowtiles;
-  int32_t window;  // sliding window in keys (0: none)
+  int32_t window;    // sliding window in keys (0: none)
+  int32_t box_rows;  // rows per K/V box: 16, 32, 64 or 128, dividing block_size
   float scale_log2;
 };
 
@@ -195,12 +198,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     setmaxnreg_dec<kOtherRegs>();
     if (warp == kProducerWarp) {
       // ------------------------------------------------------------ TMA producer
-      // Lane b < 8 owns the b-th 16-row box of every KV tile: it reads that
-      // box's block-table entry one tile ahead (the read overlaps the wait
-      // for a free stage) and issues the box's copies; lane 0 arms the
+      // Lane b < kBN / box_rows owns the b-th box of every KV tile: it reads
+      // that box's block-table entry one tile ahead (the read overlaps the
+      // wait for a free stage) and issues the box's copies; lane 0 arms the
       // barriers. K and V stages are released separately: K(j) once every
       // S = Q K(j)^T is done, V(j) once every P.V(j) is.
-      constexpr int kBoxes = kBN / kBoxRows;
+      const int box_rows = p.box_rows;
+      const int n_boxes = kBN / box_rows;
       if (lane == 0) {
         prefetch_tensormap(&q_map);
         prefetch_tensormap(&k_map);
@@ -218,8 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int32_t *table = p.block_tables + static_cast<int64_t>(s) * p.max_blocks;
-      auto box_key = [&](int j) { return j * kBN + lane * kBoxRows; };
-      auto has_box = [&](int j) { return lane < kBoxes && j < n_max && box_key(j) < Lk; };
+      auto box_key = [&](int j) { return j * kBN + lane * box_rows; };
+      auto has_box = [&](int j) { return lane < n_boxes && j < n_max && box_key(j) < Lk; };
       int32_t next_blk = has_box(j_start) ? __ldg(table + box_key(j_start) / p.block_size) : -1;
       bool good = true;
       for (int jj = 0; jj < n_steps; ++jj) {
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             row = blk * p.block_size + box_key(j) % p.block_size;
         }
         const uint32_t bytes =
-            __popc(__ballot_sync(0xffffffffu, row >= 0)) * 2u * kBoxRows * 128u;
+            __popc(__ballot_sync(0xffffffffu, row >= 0)) * 2u * box_rows * 128u;
         if (jj >= kStages &&
             !__all_sync(0xffffffffu, wait_(bar(kBarKEmpty + st), ((jj >> 1) - 1) & 1, abort))) {
           good = false;
@@ -243,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull + st), bytes);
         __syncwarp();
-        const uint32_t kdst = sK + st * kTileBytes + lane * kBoxRows * 128;
+        const uint32_t kdst = sK + st * kTileBytes + lane * box_rows * 128;
         if (row >= 0) {
           tma_load_3d(kdst, &k_map, bar(kBarKFull + st), 0, g, row);
           tma_load_3d(kdst + kHalfBytes, &k_map, bar(kBarKFull + st), 64, g, row);
@@ -255,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) mbar_arrive_expect_tx(bar(kBarVFull + st), bytes);
         __syncwarp();
-        const uint32_t vdst = sV + st * kTileBytes + lane * kBoxRows * 128;
+        const uint32_t vdst = sV + st * kTileBytes + lane * box_rows * 128;
         if (row >= 0) {
           tma_load_3d(vdst, &v_map, bar(kBarVFull + st), 0, g, row);
           tma_load_3d(vdst + kHalfBytes, &v_map, bar(kBarVFull + st), 64, g, row);
@@ -303,15 +307,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       // has steps 0 .. n_tiles[t] - j_start - 1 (none if that is not positive).
       bool good = wait_(bar(kBarQ), 0, abort);
       int v_ready = -1;  // last step whose V is resident (and tail-zeroed)
+      // This thread shares its SM sub-partition with two softmax warps, which
+      // take most issue slots while they run: every instruction here delays
+      // the next MMA. So the operand descriptors are built once, as 32-bit
+      // low halves over one common high half (all have a 1024-byte stride
+      // between 8-row groups and 128-byte swizzle), and each MMA adds a
+      // constant to the start-address field (address / 16 in the low 14 bits;
+      // no shared-memory address carries out of it).
+      const uint32_t desc_hi = static_cast<uint32_t>(smem_desc_sw128(sQ, 16, 1024) >> 32);
+      auto lo = [](uint64_t d) { return static_cast<uint32_t>(d); };
+      const uint32_t q_lo0 = lo(smem_desc_sw128(sQ, 16, 1024));
+      const uint32_t q_lo1 = lo(smem_desc_sw128(sQ + kTileBytes, 16, 1024));
+      const uint32_t k_lo0 = lo(smem_desc_sw128(sK, 16, 1024));
+      const uint32_t k_lo1 = lo(smem_desc_sw128(sK + kTileBytes, 16, 1024));
+      const uint32_t v_lo0 = lo(smem_desc_sw128(sV, kHalfBytes, 1024));
+      const uint32_t v_lo1 = lo(smem_desc_sw128(sV + kTileBytes, kHalfBytes, 1024));
       auto issue_s = [&](int t, int jj) -> bool {
         const int st = jj & 1;
         if (!wait_(bar(kBarKFull + st), (jj >> 1) & 1, abort)) return false;
         const uint32_t tS = tmem + t * kBN;
+        const uint32_t qd = t ? q_lo1 : q_lo0;
+        const uint32_t kd = st ? k_lo1 : k_lo0;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_bf16_ss(tS, smem_desc_sw128(sQ + t * kTileBytes + off, 16, 1024),
-                      smem_desc_sw128(sK + st * kTileBytes + off, 16, 1024), kIdescQK, kk > 0);
+          const uint32_t off16 = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(tS, qd + off16, kd + off16, desc_hi, kIdescQK, kk > 0);
         }
         mma_commit(bar(kBarS + t));
         return true;
@@ -331,12 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t tP = tmem + t * kBN;             // P over the first 64 columns of S_t
         const uint32_t tO = tmem + 2 * kBN + t * kD;
+        const uint32_t vd = st ? v_lo1 : v_lo0;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          mma_bf16_ts(tO, tP + kk * 8,
-                      smem_desc_sw128(sV + st * kTileBytes + kk * 16 * 128, kHalfBytes, 1024),
-                      kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_bf16_ts(tO, tP + kk * 8, vd + ((kk * 16 * 128) >> 4), desc_hi, kIdescPV,
+                      (jj > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar(kBarO + t));
         return true;
       };
@@ -570,6 +589,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
   const int rows_per_cta = G >= 2 ? kBM : 2 * kBM;
   p.n_rowtiles = (a.max_seqlen_q + rows_per_cta - 1) / rows_per_cta;
   p.window = a.window;
+  p.box_rows = a.box_rows;
   p.scale_log2 = a.scale_log2;
   dim3 grid(p.n_rowtiles, G >= 2 ? a.num_q_heads / 2 : a.num_q_heads, a.num_seqs);
   return p.window > 0 ? launch_instance<true>(grid, q_map, k_map, v_map, p, stream)
