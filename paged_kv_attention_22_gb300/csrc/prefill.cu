@@ -72,6 +72,7 @@ constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, 0, 0);  // A=Q K-major, B
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, 0, 1);   // A=P (TMEM), B=V MN-major
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kLazyMax = 8.0f;  // log2 units the running maximum may lag
+constexpr float kLazyBound = 256.0f;  // 2^kLazyMax: the largest tile sum taken as is
 
 struct PrefillParams {
   const int32_t *cu_q, *cu_k, *block_tables;
@@ -395,9 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Running maximum m (log2 units) and two running sums: l of the fp32
     // probabilities, for the lse, and lr of the same probabilities rounded to
     // bf16 as the P.V product sees them, which normalises the output. The
-    // maximum is lazy: a row keeps its m until a tile's logits exceed it by
-    // more than kLazyMax, so probabilities stay below 2^kLazyMax and O is
-    // rescaled only when some row of the warp passes that bound. Dividing by
+    // maximum is lazy: a row keeps its m while a tile's probabilities sum to
+    // at most 2^kLazyMax, so no probability exceeds that bound and O is
+    // rescaled only when some row of the warp passes it. Dividing by
     // the sum of the rounded probabilities keeps the output a convex
     // combination of the V rows with the weights the tensor core used, so a
     // large probability rounded to bf16 costs no more than it does under an
@@ -437,71 +438,92 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c >= keep) x[c] = 0xFF800000u;
         }
       }
-      // row max of the raw logits (the scale is positive): eight chains of
-      // three-input maxima
-      float a[8];
+      // P = 2^(x * scale - mm), packed two per column over the first 64
+      // columns of S_t (all of S is already in registers); ts and tr get the
+      // tile's sums of the fp32 and of the bf16-rounded probabilities
+      auto exps = [&](float mm, float &ts, float &tr) {
+        const uint64_t nm = f32x2(-mm, -mm);
+        uint64_t s0 = 0, s1 = 0;
+        float r0l = 0.f, r0h = 0.f, r1l = 0.f, r1h = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(x[i]);
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[32];
 #pragma unroll
-      for (int c = 8; c < kBN; c += 16)
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          a[i] = fmax3(a[i], __uint_as_float(x[c + i]), __uint_as_float(x[c + 8 + i]));
-      const float mx = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
-      const float mxs = mx * p.scale_log2;  // -inf stays -inf
-
-      if (jj == 0) {
-        // nothing is in O yet; without a window every row sees key 0
-        m = kWindowed ? fmaxf(mxs, kFloor) : mxs;
-      } else if (__any_sync(0xffffffffu, mxs > m + kLazyMax)) {
-        // P.V of the previous step is complete (this S was issued after it): rescale
-        // the O rows in TMEM. The accesses are warp-wide, so the whole warp
-        // takes the new maxima.
-        const float m_new = fmaxf(m, mxs);
-        const float alpha = fast_exp2(m - m_new);
-        // 32 columns at a time: all of S is held in registers meanwhile
-#pragma unroll 1
-        for (int c = 0; c < kD; c += 32) {
-          uint32_t o[32];
-          tmem_ld32(tO + c, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + c, o);
+          for (int c = 0; c < 32; ++c) {
+            const int k = hf * 64 + 2 * c;
+            const uint64_t e =
+                fma2(f32x2(__uint_as_float(x[k]), __uint_as_float(x[k + 1])), scl, nm);
+            const float p0 = fast_exp2(f32x2_lo(e)), p1 = fast_exp2(f32x2_hi(e));
+            pk[c] = pack_bf16x2(p0, p1);
+            if (c & 1) {
+              add2(s1, f32x2(p0, p1));
+              add_bf16x2_to_f32(r1l, r1h, pk[c]);
+            } else {
+              add2(s0, f32x2(p0, p1));
+              add_bf16x2_to_f32(r0l, r0h, pk[c]);
+            }
+          }
+          tmem_st32(tS + hf * 32, pk);
         }
-        tmem_wait_st();
-        l *= alpha;
-        lr *= alpha;
-        m = m_new;
-      }
-
-      // P = 2^(x * scale - m), packed two per column over the first 64
-      // columns of S_t (all of S is already in registers)
-      const uint64_t nm = f32x2(-m, -m);
-      uint64_t s0 = 0, s1 = 0, r0 = 0, r1 = 0;
+        add2(s0, s1);
+        ts = f32x2_lo(s0) + f32x2_hi(s0);
+        tr = (r0l + r1l) + (r0h + r1h);
+      };
+      // First with the row's current maximum, without looking for a larger
+      // one: if no row of the warp then has a tile sum above 2^kLazyMax, no
+      // probability exceeds that bound either and the tile is done. Otherwise
+      // (some logit lies more than a little above m; an infinite sum included)
+      // the warp takes the exact maximum, rescales O and recomputes P over
+      // what it wrote. The first tile of a row always takes the maximum.
+      float ts, tr;
+      bool exact = jj == 0;
+#pragma unroll 1
+      for (;;) {
+        if (exact) {
+          // row max of the raw logits (the scale is positive): eight chains
+          // of three-input maxima
+          float a[8];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pk[32];
+          for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(x[i]);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int k = hf * 64 + 2 * c;
-          const uint64_t e = fma2(f32x2(__uint_as_float(x[k]), __uint_as_float(x[k + 1])), scl, nm);
-          const float p0 = fast_exp2(f32x2_lo(e)), p1 = fast_exp2(f32x2_hi(e));
-          pk[c] = pack_bf16x2(p0, p1);
-          if (c & 1) {
-            add2(s1, f32x2(p0, p1));
-            add2(r1, f32x2(bf16lo(pk[c]), bf16hi(pk[c])));
+          for (int c = 8; c < kBN; c += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              a[i] = fmax3(a[i], __uint_as_float(x[c + i]), __uint_as_float(x[c + 8 + i]));
+          const float mx =
+              fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+          const float mxs = mx * p.scale_log2;  // -inf stays -inf
+          if (jj == 0) {
+            // nothing is in O yet; without a window every row sees key 0
+            m = kWindowed ? fmaxf(mxs, kFloor) : mxs;
           } else {
-            add2(s0, f32x2(p0, p1));
-            add2(r0, f32x2(bf16lo(pk[c]), bf16hi(pk[c])));
+            // P.V of the previous step is complete (this S was issued after
+            // it): rescale the O rows in TMEM. The accesses are warp-wide, so
+            // the whole warp takes its new maxima.
+            const float m_new = fmaxf(m, mxs);
+            const float alpha = fast_exp2(m - m_new);
+            // 32 columns at a time: all of S is held in registers meanwhile
+#pragma unroll 1
+            for (int c = 0; c < kD; c += 32) {
+              uint32_t o[32];
+              tmem_ld32(tO + c, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tO + c, o);
+            }
+            tmem_wait_st();
+            l *= alpha;
+            lr *= alpha;
+            m = m_new;
           }
         }
-        tmem_st32(tS + hf * 32, pk);
+        exps(m, ts, tr);
+        if (exact || !__any_sync(0xffffffffu, !(ts <= kLazyBound))) break;
+        exact = true;
       }
-      add2(s0, s1);
-      add2(r0, r1);
-      l += f32x2_lo(s0) + f32x2_hi(s0);
-      lr += f32x2_lo(r0) + f32x2_hi(r0);
+      l += ts;
+      lr += tr;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarP + t));

@@ -389,6 +389,18 @@ __device__ __forceinline__ void add2(uint64_t &acc, uint64_t b) {
   asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(b));
 }
 
+// acc_lo += the low bf16 of w, acc_hi += its high bf16, each widened exactly
+// to fp32 and added with round-to-nearest (the sm_100 mixed-precision add; the
+// same results as widening first and adding in fp32).
+__device__ __forceinline__ void add_bf16x2_to_f32(float &acc_lo, float &acc_hi, uint32_t w) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.bf16 %0, l, %0;\n\t"
+      "add.rn.f32.bf16 %1, h, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(w));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
