@@ -363,3 +363,35 @@ def test_fused_store_rejects_unknown_flags():
         q.shape[0], 16, 8, 128, case.block_size, case.num_blocks, ctypes.c_float(case.scale), 0,
         P(out.data_ptr()), None, P(ws.data_ptr()), ws.numel(), 0x2, None)
     assert rc == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_decode_workspace_reused_across_cut_structures():
+    """One workspace, never cleared, through calls whose CTA ranges cut
+    different pairs into different numbers of pieces, with one CTA per SM and
+    with one unit per CTA (every pair cut into as many pieces as it has
+    units)."""
+    for ctas in (0, 1000):
+        pkv.decode_set_config(ctas, 0)
+        try:
+            ws = pkv.new_decode_workspace(6, 16, 8, 128, 4096)
+            ws.fill_(255)
+            for i, ctx in enumerate([[77, 300, 1], [4096, 3, 640, 17, 900, 2], [16, 32],
+                                     [300, 301, 302], [1, 1, 1, 1, 1, 1], [2000, 640]]):
+                case = W.decode_case(f"reuse{i}", 60 + i, ctx, block_size=64,
+                                     num_blocks=6 * 65, blocks_per_seq=65)
+                st = case.step
+                kc, vc = gpu_pool(case)
+                gpu_store(case.history, kc, vc)
+                gpu_store(st.new, kc, vc)
+                q = dev_bf16(st.q)
+                out = torch.full_like(q, float("nan"))  # a row not written fails below
+                out, lse = pkv.paged_decode_attn(q, kc, vc, dev_i32(case.block_tables),
+                                                 dev_i32(st.context_lens), st.max_context_len,
+                                                 case.scale, out=out, workspace=ws)
+                assert pkv.check_device_errors() == 0
+                ref = oracle_run(case)
+                assert_close(out.double().cpu().numpy(), lse.double().cpu().numpy(),
+                             ref["out"], ref["lse"], f"{case.name} ctas {ctas}")
+        finally:
+            pkv.decode_set_config(0, 0)
+
