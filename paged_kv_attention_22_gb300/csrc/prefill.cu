@@ -12,9 +12,9 @@
 //   warp 8     TMA producer: both Q tiles once, then K and V tiles of 128 keys,
 //              two stages deep, 128-byte swizzled. A tile is copied as boxes of
 //              the largest of 128, 64, 32, 16 rows that divides the block size
-//              (a box never crosses a cache block): each copy costs the TMA
-//              unit a fixed overhead, so one 128-row box per column half
-//              streams far faster than eight 16-row ones.
+//              (a box never crosses a cache block): fewer, larger copies
+//              (one 128-row box per column half streams from L2 about twice
+//              as fast per SM as eight 16-row boxes).
 //   warp 9     MMA issuer. TMEM holds S_t (128 fp32 columns) and O_t (128) for
 //              each tile t. Per KV tile j and query tile t: S_t = Q_t K_j^T
 //              (A and B from shared memory), then, once the softmax has
