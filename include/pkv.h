@@ -40,7 +40,7 @@
  *
  * Errors. Arguments the host can see are checked before anything is enqueued:
  * PKV_ERR_INVALID_ARG (null pointer, negative size, inconsistent shape),
- * PKV_ERR_UNSUPPORTED (a shape this build has no kernel for),
+ * PKV_ERR_UNSUPPORTED (a shape this library has no kernel for),
  * PKV_ERR_WORKSPACE_TOO_SMALL. A failing CUDA call gives PKV_ERR_CUDA and
  * pkv_last_cuda_error() names it (thread-local). Values that live on the device
  * (slots, table entries, lengths) are checked by the kernels: an invalid one
