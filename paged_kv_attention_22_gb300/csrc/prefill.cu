@@ -45,7 +45,6 @@ constexpr int kD = 128;
 constexpr int kBM = 128;                       // query rows per tile
 constexpr int kBN = 128;                       // keys per KV tile
 constexpr int kTiles = 2;                      // query tiles per CTA
-constexpr int kRowBlock = 4;                   // row tiles per block of the CTA order
 constexpr int kHalfBytes = 128 * 128;          // 128 rows x 64 bf16 (one swizzle column group)
 constexpr int kTileBytes = 2 * kHalfBytes;     // 128 rows x 128 bf16
 constexpr int kStages = 2;
@@ -106,27 +105,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // CTA -> (sequence, head pair, row tile). The heaviest row tiles (the last
-  // ones: they see the most keys) go first, in blocks of kRowBlock row tiles
-  // of one head pair at a time over all pairs and sequences: longest first
-  // shortens the grid's tail, and a block's CTAs share most of their K/V tiles
-  // in L2. When the row tiles do not divide into blocks: row tiles of one
-  // head pair in a row, heaviest first.
-  int s, pair, rt;
-  {
-    const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-    if (p.n_rowtiles % kRowBlock == 0) {
-      const int per_block = gridDim.y * gridDim.z * kRowBlock;
-      const int grp = (lin % per_block) / kRowBlock;
-      rt = p.n_rowtiles - 1 - ((lin / per_block) * kRowBlock + lin % kRowBlock);
-      pair = grp % gridDim.y;
-      s = grp / gridDim.y;
-    } else {
-      rt = p.n_rowtiles - 1 - static_cast<int>(blockIdx.x);
-      pair = blockIdx.y;
-      s = blockIdx.z;
-    }
-  }
+  // CTA -> (sequence, head pair, row tile): the heaviest row tiles (the last
+  // ones, which see the most keys) of every head pair and sequence first, the
+  // lightest last, so that the grid's tail holds the shortest CTAs.
+  const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  const int per_rt = gridDim.y * gridDim.z;  // CTAs per row tile index
+  const int rt = p.n_rowtiles - 1 - lin / per_rt;
+  const int pair = (lin % per_rt) % gridDim.y;
+  const int s = (lin % per_rt) / gridDim.y;
   const int G = p.num_q_heads / p.num_kv_heads;
 
   griddep_wait();  // inputs written by the previous kernel are visible from here on
