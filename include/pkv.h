@@ -45,9 +45,17 @@
  * pkv_last_cuda_error() names it (thread-local). Values that live on the device
  * (slots, table entries, lengths) are checked by the kernels: an invalid one
  * skips the access it would have made and raises a bit of the device error
- * word (PKV_DEVERR_*), read with pkv_check_device_errors. Outputs that depend
- * on an invalid value are undefined; nothing outside the given buffers is
- * touched.
+ * word (PKV_DEVERR_*), read with pkv_check_device_errors (which blocks) or
+ * pkv_read_device_errors_async (which does not). Outputs that depend on an
+ * invalid value are undefined; nothing outside the given buffers is touched.
+ *
+ * Timeouts are sticky. Every wait inside a kernel is bounded; a kernel that
+ * gives up raises PKV_DEVERR_TIMEOUT. From then on every later decode call
+ * (fused store included) and prefill call on that device returns PKV_OK but
+ * skips all its work, leaving its outputs (and, for the fused call, the cache)
+ * untouched, until the word is cleared by pkv_check_device_errors. An engine
+ * that runs these calls inside CUDA graphs and never synchronises should
+ * append pkv_read_device_errors_async to its step and act on the bit.
  */
 #ifndef PKV_H
 #define PKV_H
@@ -94,7 +102,11 @@ const char *pkv_last_cuda_error(void);
 
 /*
  * KV store: the slot-mapping scatter of the new tokens' K/V rows into the
- * cache. k_cache[slot_mapping[t]] = k[t] and v_cache[slot_mapping[t]] = v[t]
+ * paged cache (the engine's KV block manager hands out the cache slots: "How
+ * lunaryes/nano-vllm works", Components: KV Block Manager, and Connections:
+ * "Scheduler -> KV Block Manager: allocates cached blocks"; the cache is the
+ * paged KV cache of the nano-vllm-rs README, "GGUF Models").
+ * k_cache[slot_mapping[t]] = k[t] and v_cache[slot_mapping[t]] = v[t]
  * for every t with slot_mapping[t] >= 0 (all H_kv * D values of the row, bit
  * for bit); -1 skips the token (the block manager gave it no slot, as for
  * tokens of a cached prefix). Two tokens with the same non-negative slot in one
@@ -223,7 +235,11 @@ void pkv_decode_set_config(int32_t ctas, int32_t variant);
  *     PKV_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture. The address is kept for the life of the
+ *     process: a cudaDeviceReset of that device afterwards is not supported.
+ *   - Without a usable device the call returns PKV_ERR_CUDA (with
+ *     pkv_last_cuda_error set); sizes that no decode call accepts return
+ *     PKV_ERR_INVALID_ARG.
  *   - Every call on a device shares that device's one array, which keeps the
  *     last call's contents; nothing in it needs to start at zero. Calls that
  *     can overlap on the GPU (for example on two streams with no ordering
@@ -247,7 +263,11 @@ pkv_status pkv_paged_decode_attn_noalloc(const void *q, const void *k_cache, con
 size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t max_seqlen_q);
 
 /*
- * Varlen causal prefill attention over the paged cache, with prefix caching.
+ * Varlen causal prefill attention over the paged cache, with prefix caching
+ * (nano-vllm-sansho README, "Key Features": prefix caching; "How
+ * lunaryes/nano-vllm works", Connections: the block manager allocates cached
+ * blocks, which a later prompt with the same leading tokens reads instead of
+ * recomputing them).
  * Segment s has Lq = cu_seqlens_q[s+1] - cu_seqlens_q[s] query tokens
  * (rows cu_seqlens_q[s] .. of q) and Lk = cu_seqlens_k[s+1] - cu_seqlens_k[s]
  * keys, read through block_tables[s]; the queries are the last Lq of the Lk
@@ -281,9 +301,32 @@ pkv_status pkv_paged_prefill_attn(const void *q, const void *k_cache, const void
 /*
  * Synchronise `stream`, then return in *flags_out the OR of the device error
  * words of every kernel of this library on the current device, and clear
- * them. For tests and debugging: it blocks the host.
+ * them. It blocks the host; it is also the only way to clear the words, and
+ * so to end the skip that a PKV_DEVERR_TIMEOUT starts.
  */
 pkv_status pkv_check_device_errors(void *stream, uint32_t *flags_out);
+
+/*
+ * Non-blocking readout of the device error words: enqueues on `stream` a
+ * one-thread kernel that writes the OR of the error words of every kernel of
+ * this library on the current device into *host_flags, in stream order after
+ * the work enqueued before it. The words are not cleared. host_flags must be
+ * page-locked host memory (cudaHostAlloc, cudaMallocHost or cudaHostRegister)
+ * that the device can write; other memory gives PKV_ERR_INVALID_ARG. The value
+ * is there once that kernel has completed (for example after an event
+ * recorded behind it). Capturable; make the first call on a device (which
+ * looks up the words' addresses) before any stream capture.
+ */
+pkv_status pkv_read_device_errors_async(uint32_t *host_flags, void *stream);
+
+/*
+ * Raise bits of the device error words from the host, in stream order, as a
+ * kernel that met the condition would. For tests of an engine's error
+ * handling, for instance of the skip that follows PKV_DEVERR_TIMEOUT, without
+ * making any kernel wait or fault. Bits outside PKV_DEVERR_* give
+ * PKV_ERR_INVALID_ARG.
+ */
+pkv_status pkv_raise_device_errors(uint32_t flags, void *stream);
 
 #ifdef __cplusplus
 }

@@ -91,6 +91,10 @@ def lib():
     L.pkv_paged_prefill_attn.restype = ctypes.c_int
     L.pkv_check_device_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     L.pkv_check_device_errors.restype = ctypes.c_int
+    L.pkv_read_device_errors_async.argtypes = [P, P]
+    L.pkv_read_device_errors_async.restype = ctypes.c_int
+    L.pkv_raise_device_errors.argtypes = [ctypes.c_uint32, P]
+    L.pkv_raise_device_errors.restype = ctypes.c_int
     pi32 = ctypes.POINTER(ctypes.c_int32)
     L.pkv_bm_create.argtypes = [i32, i32]
     L.pkv_bm_create.restype = P
@@ -334,6 +338,24 @@ def check_device_errors(stream=None) -> int:
     _check(lib().pkv_check_device_errors(_stream(stream), ctypes.byref(flags)),
            "pkv_check_device_errors")
     return int(flags.value)
+
+
+def read_device_errors_async(host_flags, stream=None) -> None:
+    """Enqueue a non-blocking readout of the OR of the kernels' device error
+    words into host_flags, a pinned (page-locked) CPU int32/uint32 tensor of
+    at least one element; its first element holds the value once the work
+    enqueued before this call on the stream has completed. Nothing is cleared."""
+    if not isinstance(host_flags, torch.Tensor) or host_flags.is_cuda \
+            or host_flags.dtype not in (torch.int32,) or host_flags.numel() < 1:
+        raise TypeError("host_flags must be a CPU int32 tensor")
+    _check(lib().pkv_read_device_errors_async(_ptr(host_flags), _stream(stream)),
+           "pkv_read_device_errors_async")
+
+
+def raise_device_errors(flags: int, stream=None) -> None:
+    """Raise bits of the device error words from the host, in stream order (for
+    tests of error handling)."""
+    _check(lib().pkv_raise_device_errors(int(flags), _stream(stream)), "pkv_raise_device_errors")
 
 
 class BlockManager:

@@ -16,11 +16,21 @@ namespace {
 
 thread_local char g_last_cuda_error[256] = "";
 
+}  // namespace
+
+namespace pkv {
+
 pkv_status cuda_fail(cudaError_t e, const char *where) {
   snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s (%s)", where,
            cudaGetErrorName(e), cudaGetErrorString(e));
   return PKV_ERR_CUDA;
 }
+
+}  // namespace pkv
+
+namespace {
+
+using pkv::cuda_fail;
 
 pkv_status cu_fail(CUresult r, const char *where) {
   snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: CUresult %d", where,
@@ -32,6 +42,10 @@ pkv_status cu_fail(CUresult r, const char *where) {
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
+
+}  // namespace
+
+namespace pkv {
 
 pkv_status current_sm_count(int *sms) {
   int dev = 0;
@@ -56,6 +70,12 @@ pkv_status current_sm_count(int *sms) {
   *sms = n;
   return PKV_OK;
 }
+
+}  // namespace pkv
+
+namespace {
+
+using pkv::current_sm_count;
 
 // ---------------------------------------------------------------- TMA descriptors
 
@@ -331,6 +351,64 @@ pkv_status decode_common(const void *k_new, const void *v_new, const int32_t *sl
 
 }  // namespace
 
+namespace {
+
+// The device error words of the three kernel files on one device.
+struct ErrorWords {
+  uint32_t *w[3];
+};
+std::mutex g_words_mutex;
+ErrorWords g_words[kMaxDevices];
+bool g_words_set[kMaxDevices] = {};
+
+// Addresses of the error words on the current device, looked up once per
+// device and process.
+pkv_status error_words(ErrorWords *out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice, "device index");
+  std::lock_guard<std::mutex> lock(g_words_mutex);
+  if (!g_words_set[dev]) {
+    ErrorWords w;
+    if ((e = pkv::kv_store_error_word(&w.w[0])) != cudaSuccess ||
+        (e = pkv::decode_error_word(&w.w[1])) != cudaSuccess ||
+        (e = pkv::prefill_error_word(&w.w[2])) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress (device error words)");
+    g_words[dev] = w;
+    g_words_set[dev] = true;
+  }
+  *out = g_words[dev];
+  return PKV_OK;
+}
+
+// A one-thread launch in stream order (no programmatic dependent launch: it
+// starts after the previous kernel on the stream has completed).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_one_thread(void (*kernel)(KArgs...), void *stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// One thread: *dst = the OR of the three words (dst may be a mapped host word).
+__global__ void read_errors_kernel(ErrorWords w, uint32_t *dst) {
+  uint32_t v = 0;
+#pragma unroll
+  for (int i = 0; i < 3; ++i) v |= *reinterpret_cast<volatile uint32_t *>(w.w[i]);
+  *reinterpret_cast<volatile uint32_t *>(dst) = v;
+}
+
+// One thread: OR `bits` into each of the three words.
+__global__ void raise_errors_kernel(ErrorWords w, uint32_t bits) {
+#pragma unroll
+  for (int i = 0; i < 3; ++i) atomicOr(w.w[i], bits);
+}
+
+}  // namespace
+
 extern "C" {
 
 pkv_status pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
@@ -430,6 +508,41 @@ pkv_status pkv_paged_prefill_attn(const void *q, const void *k_cache, const void
     return st;
   cudaError_t e = pkv::launch_prefill(a, qmap, kmap, vmap, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return PKV_OK;
+}
+
+pkv_status pkv_read_device_errors_async(uint32_t *host_flags, void *stream) {
+  if (host_flags == nullptr) return PKV_ERR_INVALID_ARG;
+  // only page-locked host memory with a device mapping is written by the
+  // kernel; anything else is rejected before a launch
+  cudaPointerAttributes attr{};
+  cudaError_t e = cudaPointerGetAttributes(&attr, host_flags);
+  if (e != cudaSuccess || attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) {
+    if (e != cudaSuccess) {
+      cuda_fail(e, "cudaPointerGetAttributes (host_flags)");
+      (void)cudaGetLastError();  // an argument error: leave no pending runtime error behind
+    }
+    return PKV_ERR_INVALID_ARG;
+  }
+  uint32_t *dst = static_cast<uint32_t *>(attr.devicePointer);
+  ErrorWords w;
+  pkv_status st = error_words(&w);
+  if (st != PKV_OK) return st;
+  if ((e = launch_one_thread(read_errors_kernel, stream, w, dst)) != cudaSuccess)
+    return cuda_fail(e, "error readout launch");
+  return PKV_OK;
+}
+
+pkv_status pkv_raise_device_errors(uint32_t flags, void *stream) {
+  if ((flags & ~(PKV_DEVERR_SLOT | PKV_DEVERR_BLOCK | PKV_DEVERR_CONTEXT | PKV_DEVERR_SEQLENS |
+                 PKV_DEVERR_TIMEOUT)) != 0)
+    return PKV_ERR_INVALID_ARG;
+  ErrorWords w;
+  pkv_status st = error_words(&w);
+  if (st != PKV_OK) return st;
+  if (flags == 0) return PKV_OK;
+  const cudaError_t e = launch_one_thread(raise_errors_kernel, stream, w, flags);
+  if (e != cudaSuccess) return cuda_fail(e, "error raise launch");
   return PKV_OK;
 }
 

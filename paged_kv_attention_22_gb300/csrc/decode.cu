@@ -817,6 +817,10 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
   }
 }
 
+cudaError_t decode_error_word(uint32_t **word) {
+  return cudaGetSymbolAddress(reinterpret_cast<void **>(word), g_decode_errors);
+}
+
 cudaError_t take_decode_errors(cudaStream_t stream, uint32_t *flags) {
   uint32_t v = 0;
   cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_decode_errors, sizeof v, 0,

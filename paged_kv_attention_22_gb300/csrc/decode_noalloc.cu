@@ -25,16 +25,22 @@ std::mutex g_setup_mutex;
 void *g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up once per
-// device. In host code the array's name is only a host-side stand-in, so the
-// kernels must be given this address, never the name.
+// device and process (a later cudaDeviceReset of that device is not supported:
+// the address kept here would outlive the context it belongs to). In host code
+// the array's name is only a host-side stand-in, so the kernels must be given
+// this address, never the name.
 pkv_status scratch_for_current_device(void **ptr) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return pkv::cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return pkv::cuda_fail(cudaErrorInvalidDevice, "device index");
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (g_scratch_ptr[dev] == nullptr) {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return PKV_ERR_CUDA;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "cudaGetSymbolAddress (decode scratch)");
+    if (p == nullptr)
+      return pkv::cuda_fail(cudaErrorInvalidSymbol, "cudaGetSymbolAddress (decode scratch)");
     g_scratch_ptr[dev] = p;
   }
   *ptr = g_scratch_ptr[dev];
@@ -49,13 +55,17 @@ extern "C" pkv_status pkv_paged_decode_attn_noalloc(
     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
     int32_t block_size, int64_t num_blocks, float scale, int32_t sliding_window, void *out,
     float *lse, void *stream) {
+  // the scratch size depends on the device: without a usable one this is a
+  // CUDA error (recorded for pkv_last_cuda_error), not an argument error
+  int sms = 0;
+  pkv_status st = pkv::current_sm_count(&sms);
+  if (st != PKV_OK) return st;
   const size_t need =
       pkv_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len);
-  if (need == 0) return PKV_ERR_INVALID_ARG;
+  if (need == 0) return PKV_ERR_INVALID_ARG;  // sizes no decode call accepts
   if (need > kScratchBytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
   void *scratch = nullptr;
-  const pkv_status st = scratch_for_current_device(&scratch);
-  if (st != PKV_OK) return st;
+  if ((st = scratch_for_current_device(&scratch)) != PKV_OK) return st;
   // Nothing in the scratch needs to start at zero: every partial result the
   // call reads back, it writes first.
   return pkv_paged_decode_attn(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,

@@ -7,7 +7,17 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "pkv.h"
+
 namespace pkv {
+
+// Record a failed CUDA call as this thread's last error (pkv_last_cuda_error)
+// and return PKV_ERR_CUDA.
+pkv_status cuda_fail(cudaError_t e, const char *where);
+
+// SM count of the current device (cached per device); PKV_ERR_CUDA, with the
+// error recorded, without a usable device or on a GPU older than sm_100.
+pkv_status current_sm_count(int *sms);
 
 // Launch with programmatic stream serialization (programmatic dependent
 // launch), so a kernel's launch and prologue overlap the previous kernel's
@@ -41,6 +51,8 @@ struct KvStoreArgs {
 };
 cudaError_t launch_kv_store(const KvStoreArgs &a, cudaStream_t stream);
 cudaError_t take_kv_store_errors(cudaStream_t stream, uint32_t *flags);
+// Device address of the kernel file's error word on the current device.
+cudaError_t kv_store_error_word(uint32_t **word);
 
 // ---------------------------------------------------------------- decode
 constexpr int kDecodeChunk = 16;          // keys per unit (one TMA box of all heads of a group)
@@ -88,6 +100,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
                           const CUtensorMap &kn_map, const CUtensorMap &vn_map,
                           cudaStream_t stream);
 cudaError_t take_decode_errors(cudaStream_t stream, uint32_t *flags);
+cudaError_t decode_error_word(uint32_t **word);
 
 // ---------------------------------------------------------------- prefill
 struct PrefillArgs {
@@ -115,5 +128,6 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
                            const CUtensorMap &k_map, const CUtensorMap &v_map,
                            cudaStream_t stream);
 cudaError_t take_prefill_errors(cudaStream_t stream, uint32_t *flags);
+cudaError_t prefill_error_word(uint32_t **word);
 
 }  // namespace pkv

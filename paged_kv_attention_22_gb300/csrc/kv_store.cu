@@ -83,6 +83,10 @@ cudaError_t launch_kv_store(const KvStoreArgs &a, cudaStream_t stream) {
                     a.slot_mapping, a.num_tokens, a.row_vec16, a.num_slots);
 }
 
+cudaError_t kv_store_error_word(uint32_t **word) {
+  return cudaGetSymbolAddress(reinterpret_cast<void **>(word), g_kv_store_errors);
+}
+
 cudaError_t take_kv_store_errors(cudaStream_t stream, uint32_t *flags) {
   uint32_t v = 0;
   cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_kv_store_errors, sizeof v, 0,

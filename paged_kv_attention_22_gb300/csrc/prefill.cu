@@ -624,6 +624,10 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
                       : launch_instance<false>(grid, q_map, k_map, v_map, p, stream);
 }
 
+cudaError_t prefill_error_word(uint32_t **word) {
+  return cudaGetSymbolAddress(reinterpret_cast<void **>(word), g_prefill_errors);
+}
+
 cudaError_t take_prefill_errors(cudaStream_t stream, uint32_t *flags) {
   uint32_t v = 0;
   cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_prefill_errors, sizeof v, 0,

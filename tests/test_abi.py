@@ -92,9 +92,13 @@ def test_decode_workspace_size(L):
     assert L.pkv_decode_workspace_size(64, 12, 8, 128, 640) == 0
     a = L.pkv_decode_workspace_size(64, 16, 8, 128, 640)
     if torch.cuda.is_available():
-        # grows with the sequence count, not with context length
-        assert 0 < a < L.pkv_decode_workspace_size(128, 16, 8, 128, 640)
+        # two partial-result slots per persistent CTA: the size follows the SM
+        # count and the head counts, neither the sequence count nor the context
+        assert a > 0
+        assert a == L.pkv_decode_workspace_size(128, 16, 8, 128, 640)
+        assert a == L.pkv_decode_workspace_size(1, 16, 8, 128, 640)
         assert a == L.pkv_decode_workspace_size(64, 16, 8, 128, 8193)
+        assert a < L.pkv_decode_workspace_size(64, 32, 8, 128, 640)  # G = 4 query heads per KV head
     else:
         assert a == 0  # the size depends on the device's SM count
 

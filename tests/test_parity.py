@@ -58,6 +58,19 @@ def test_prefix8k_decode_full():
     assert_close(got["out"], got["lse"], ref["out"], ref["lse"], "prefix8k decode")
 
 
+def test_prefix8k_prefill_full():
+    # the prefix-cached prefill at full size (8 x 4096 new query rows over a
+    # shared 4096-token cached prefix, 16 heads): every output element and
+    # every lse against the fp64 oracle, cache bytes over the whole pool
+    pre, _ = W.prefix8k()
+    got = gpu_run(pre)
+    ref = oracle_run(pre)
+    assert got["flags"] == 0
+    assert_cache_equal(got["kc"], got["vc"], ref["kc"], ref["vc"])
+    assert got["out"].shape == ref["out"].shape == (32768, pre.H_q, pre.D)
+    assert_close(got["out"], got["lse"], ref["out"], ref["lse"], "prefix8k prefill (every row)")
+
+
 def test_prefix8k_prefill_sampled_rows():
     pre, _ = W.prefix8k()
     got = gpu_run(pre)

@@ -139,6 +139,13 @@ def test_windowed_prefill_one_query_head_per_kv_head():
         _check_prefill(case, window)
 
 
+def test_windowed_prefix8k_prefill_full():
+    # the full-size prefix workload with the SWA-256 window: every output
+    # element and every lse against the windowed fp64 oracle
+    pre, _ = W.prefix8k()
+    _check_prefill(pre, 256)
+
+
 def test_windowed_prefix8k_decode_and_sampled_prefill_rows():
     pre, dec = W.prefix8k()
     window = 256
