@@ -644,6 +644,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
   if (U == 0) return;
   const int64_t W = decode_grid < U ? decode_grid : U;
   griddep_wait();  // the decode kernel's partials are visible from here on
+  // after a timeout (in the decode kernel just before this one, or in an
+  // earlier launch, which made that kernel skip its work) the partials are
+  // stale: write nothing, as the decode kernel did not
+  if (*reinterpret_cast<volatile uint32_t *>(&g_decode_errors) & kErrTimeout) return;
   const int64_t n_pairs = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads;
   for (int64_t pi = static_cast<int64_t>(blockIdx.x) * kMergeWarps + warp; pi < n_pairs;
        pi += static_cast<int64_t>(gridDim.x) * kMergeWarps) {
