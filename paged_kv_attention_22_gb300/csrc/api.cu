@@ -470,7 +470,6 @@ pkv_status pkv_paged_prefill_attn(const void *q, const void *k_cache, const void
                                         num_blocks, max_blocks_per_seq);
   if (st != PKV_OK) return st;
   if (total_q > 0 && (q == nullptr || out == nullptr)) return PKV_ERR_INVALID_ARG;
-  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return PKV_OK;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PKV_ERR_INVALID_ARG;
@@ -494,7 +493,16 @@ pkv_status pkv_paged_prefill_attn(const void *q, const void *k_cache, const void
   a.block_size = block_size;
   a.num_blocks = static_cast<int32_t>(num_blocks);
   a.window = sliding_window;
+  a.num_sms = sms;
   a.scale_log2 = scale * kLog2e;
+  {
+    // the kernel indexes its work items with 32-bit integers
+    const int32_t G = num_q_heads / num_kv_heads;
+    const int64_t rows_per_item = G >= 2 ? 128 : 256;
+    const int64_t n_items = (max_seqlen_q + rows_per_item - 1) / rows_per_item *
+                            (G >= 2 ? num_q_heads / 2 : num_q_heads) * num_seqs;
+    if (n_items > pkv::kMaxPrefillItems) return PKV_ERR_UNSUPPORTED;
+  }
 
   CUtensorMap qmap, kmap, vmap;
   const int64_t rows = num_blocks * block_size;

@@ -114,8 +114,12 @@ struct PrefillArgs {
   int32_t num_blocks;
   int32_t window;  // sliding window in keys (0: none)
   int32_t box_rows;  // rows per K/V TMA box: prefill_box_rows(block_size)
+  int32_t num_sms;   // SMs of the device (persistent grid)
   float scale_log2;
 };
+// Work items of one prefill call (row tiles x head pairs x sequences) are
+// indexed with 32-bit integers, with headroom for the per-CTA walk.
+constexpr int64_t kMaxPrefillItems = (int64_t{1} << 31) - (int64_t{1} << 20);
 // Rows per K/V box of the prefill kernel: the largest of 128, 64, 32, 16 that
 // divides the block size, so that a box never crosses a cache block and a
 // 128-key tile takes as few copies as the block size allows.

@@ -53,20 +53,35 @@ constexpr int kKOff = kQOff + kTiles * kTileBytes;
 constexpr int kVOff = kKOff + kStages * kTileBytes;
 constexpr int kBarOff = kVOff + kStages * kTileBytes;
 // barrier slots (8 bytes each)
-// kBarVTail: the last V tile, its rows past the segment's end zeroed
+// kBarVTail + st: the item's last V tile in stage st, its rows past the
+// segment's end zeroed; kBarQEmpty: the item's S MMAs are done with Q;
+// kBarDone: every MMA of the CTA has completed
 constexpr int kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKEmpty = 5, kBarVEmpty = 7, kBarS = 9,
-              kBarP = 11, kBarO = 13, kBarVTail = 15, kNumBars = 16;
+              kBarP = 11, kBarO = 13, kBarVTail = 15, kBarQEmpty = 17, kBarDone = 18,
+              kNumBars = 19;
 constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
 constexpr int kAbortOff = kTmemSlotOff + 8;
-constexpr int kSmemBytes = kAbortOff + 8 + 1024;  // + slack for 1024-byte alignment
+// the persistent kernel's current item as the MMA issuer needs it, published
+// by the producer before it arms the item's Q barrier: int [4] = steps of
+// tiles 0 and 1, KV steps (0: no more items), 1 if the last KV tile extends
+// past the segment's last key
+constexpr int kItemOff = kAbortOff + 8;
+constexpr int kSmemBytes = kItemOff + 32 + 1024;  // + slack for 1024-byte alignment
 // warps 0-7 softmax (warpgroup t for query tile t), warp 8 TMA producer,
 // warp 9 MMA issuer, warps 10-11 idle: three warpgroups, so that setmaxnreg
 // can move registers from the third to the two softmax warpgroups
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
-// registers per thread after the split; 2 * 216 + 72 = 3 * 168, the launch's
-// share per thread of the 64K register file for 384 threads
-constexpr int kSoftmaxRegs = 216, kOtherRegs = 72;
+// registers per thread after the split, 2 * softmax + other = 3 * 168 (the
+// launch's share per thread of the 64K register file for 384 threads): the
+// persistent kernel's producer and MMA loops also keep their walk over the
+// items in registers, which 88 holds without spills
+template <bool kPersistent>
+struct RegSplit {
+  static constexpr int kSoftmax = kPersistent ? 208 : 216;
+  static constexpr int kOther = kPersistent ? 88 : 72;
+  static_assert(2 * kSoftmax + kOther == 3 * 168, "register split");
+};
 constexpr uint32_t kTmemCols = 512;            // S0, S1, O0, O1: 128 columns each
 constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, 0, 0);  // A=Q K-major, B=K K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, 0, 1);   // A=P (TMEM), B=V MN-major
@@ -79,7 +94,8 @@ struct PrefillParams {
   __nv_bfloat16 *out;
   float *lse;
   int32_t max_blocks, num_seqs, total_q, max_seqlen_q, max_seqlen_k;
-  int32_t num_q_heads, num_kv_heads, block_size, num_blocks, n_rowtiles;
+  int32_t num_q_heads, num_kv_heads, block_size, num_blocks;
+  int32_t n_rowtiles, n_pairs, n_items;  // the item list: row tiles x head pairs x sequences
   int32_t window;    // sliding window in keys (0: none)
   int32_t box_rows;  // rows per K/V box: 16, 32, 64 or 128, dividing block_size
   float scale_log2;
@@ -94,9 +110,113 @@ __device__ __forceinline__ void fail(volatile int *abort) {
   atomicOr(&g_prefill_errors, kErrTimeout);
 }
 
+// One work item: two 128-row query tiles that share every K/V tile. With
+// grouped queries (H_q / H_kv >= 2) the two query heads of a head pair over
+// the same 128 rows; without grouping, two consecutive row tiles of one head.
+struct Item {
+  int s, q0, Lq, Lk, diag, g;
+  int head[kTiles], row0[kTiles];
+  int n_tiles[kTiles];  // KV tiles 0 .. n_tiles[t] - 1 hold the keys of tile t (0: no rows)
+  int j_start;          // first KV tile any of the rows sees (sliding window)
+  int n_steps;          // KV tiles j_start .. j_start + n_steps - 1
+};
+
+// Item `lin` of the list, heaviest first: row tiles from the last (which see
+// the most keys) to the first, each over all head pairs and sequences. False
+// for an item without work (rows past the segment, or lengths that fail the
+// checks, which `raise` reports once per sequence).
+template <bool kWindowed>
+__device__ __forceinline__ bool make_item(const PrefillParams &p, int lin, bool raise, Item &it) {
+  const int per_rt = p.n_pairs * p.num_seqs;
+  const int rt = p.n_rowtiles - 1 - lin / per_rt;
+  const int pair = (lin % per_rt) % p.n_pairs;
+  it.s = (lin % per_rt) / p.n_pairs;
+  const int G = p.num_q_heads / p.num_kv_heads;
+  it.q0 = p.cu_q[it.s];
+  const int q1 = p.cu_q[it.s + 1];
+  it.Lq = q1 - it.q0;
+  it.Lk = p.cu_k[it.s + 1] - p.cu_k[it.s];
+  if (it.q0 < 0 || it.Lq < 0 || it.Lk < it.Lq || it.Lq > p.max_seqlen_q ||
+      it.Lk > p.max_seqlen_k || q1 > p.total_q ||
+      static_cast<int64_t>(it.Lk) > static_cast<int64_t>(p.max_blocks) * p.block_size) {
+    if (raise && rt == p.n_rowtiles - 1 && pair == 0) atomicOr(&g_prefill_errors, kErrSeqlens);
+    return false;
+  }
+  if (G >= 2) {
+    it.head[0] = 2 * pair;
+    it.head[1] = 2 * pair + 1;
+    it.row0[0] = it.row0[1] = rt * kBM;
+  } else {
+    it.head[0] = it.head[1] = pair;
+    it.row0[0] = 2 * rt * kBM + kBM;  // the later (heavier) row tile first
+    it.row0[1] = 2 * rt * kBM;
+  }
+  it.g = it.head[0] / G;
+  it.diag = it.Lk - it.Lq;  // query i sees keys <= diag + i
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t) {
+    if (it.row0[t] >= it.Lq) {
+      it.n_tiles[t] = 0;
+    } else {
+      const int kv_end = it.diag + min(it.Lq, it.row0[t] + kBM);  // keys the tile needs (<= Lk)
+      it.n_tiles[t] = (kv_end + kBN - 1) / kBN;
+    }
+  }
+  const int n_max = max(it.n_tiles[0], it.n_tiles[1]);
+  // With a sliding window query i sees keys >= diag + i - window + 1: the KV
+  // tiles before the one that holds the earliest such key of the item's rows
+  // are skipped.
+  it.j_start = 0;
+  if constexpr (kWindowed) {
+    int lo = it.Lk;
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t)
+      if (it.n_tiles[t] > 0) lo = min(lo, max(0, it.diag + it.row0[t] - p.window + 1));
+    it.j_start = lo / kBN;
+  }
+  it.n_steps = n_max - it.j_start;
+  return n_max > 0;
+}
+
+// This CTA's items in order: CTA c of C takes items c, 2C - 1 - c, 2C + c, ...
+// of the heaviest-first list (rounds alternate direction, so that every CTA
+// gets a similar mix of heavy and light items).
+// Without persistence CTA c takes item c alone.
+template <bool kWindowed, bool kPersistent>
+struct ItemWalk {
+  int k = 0;         // next round to look at
+  int item_no = -1;  // index of the current item among this CTA's items with work
+  // The next item with work into `it`; false when there is none.
+  __device__ __forceinline__ bool next(const PrefillParams &p, bool raise, Item &it) {
+    const int C = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    for (;;) {
+      if (!kPersistent && k > 0) return false;
+      const int lin = k * C + ((k & 1) ? C - 1 - c : c);
+      ++k;
+      if (lin >= p.n_items) return false;
+      if (make_item<kWindowed>(p, lin, raise, it)) {
+        ++item_no;
+        return true;
+      }
+    }
+  }
+};
+
 // kWindowed: a sliding window is set (p.window > 0). The kernel without one
 // is a separate instantiation, so that it keeps no window bookkeeping at all.
-template <bool kWindowed>
+//
+// kPersistent: one CTA per SM walks its items (used with a window, where an
+// item is two or three KV steps and a CTA's fixed cost, a few microseconds of
+// set-up, pipeline fill and drain, would otherwise rival its work); else one
+// CTA per item, in the list's order (long items: the hardware's assignment of
+// CTAs to SMs as they free up balances them). Barrier phases run on across
+// items: K/V stages and the V-tail barriers count the CTA's KV steps, the S,
+// P and O barriers of tile t count that tile's steps, the Q barriers count
+// items. The next item's Q is loaded once every S MMA of the current item has
+// completed (kBarQEmpty), its first S MMAs follow the current item's last
+// P.V in issue order, and its first P.V (which overwrites O) waits for the
+// softmax warps' P, which they write only after reading the current O.
+template <bool kWindowed, bool kPersistent>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                    const __grid_constant__ CUtensorMap k_map,
@@ -105,69 +225,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // CTA -> (sequence, head pair, row tile): the heaviest row tiles (the last
-  // ones, which see the most keys) of every head pair and sequence first, the
-  // lightest last, so that the grid's tail holds the shortest CTAs.
-  const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-  const int per_rt = gridDim.y * gridDim.z;  // CTAs per row tile index
-  const int rt = p.n_rowtiles - 1 - lin / per_rt;
-  const int pair = (lin % per_rt) % gridDim.y;
-  const int s = (lin % per_rt) / gridDim.y;
-  const int G = p.num_q_heads / p.num_kv_heads;
-
-  griddep_wait();  // inputs written by the previous kernel are visible from here on
-  // a CTA gave up waiting (in this or an earlier launch): skip the work until
-  // the error word is read and cleared; decided once per CTA
-  if (__syncthreads_or(tid == 0 &&
-                       (*reinterpret_cast<volatile uint32_t *>(&g_prefill_errors) & kErrTimeout)))
-    return;
-
-  const int q0 = p.cu_q[s], q1 = p.cu_q[s + 1];
-  const int Lq = q1 - q0, Lk = p.cu_k[s + 1] - p.cu_k[s];
-  if (q0 < 0 || Lq < 0 || Lk < Lq || Lq > p.max_seqlen_q || Lk > p.max_seqlen_k ||
-      q1 > p.total_q ||
-      static_cast<int64_t>(Lk) > static_cast<int64_t>(p.max_blocks) * p.block_size) {
-    if (rt == p.n_rowtiles - 1 && pair == 0 && tid == 0) atomicOr(&g_prefill_errors, kErrSeqlens);
-    return;
-  }
-  // the two query tiles: (head, first row) each; heaviest row tiles first
-  int head[kTiles], row0[kTiles];
-  if (G >= 2) {
-    head[0] = 2 * pair;
-    head[1] = 2 * pair + 1;
-    row0[0] = row0[1] = rt * kBM;
-  } else {
-    head[0] = head[1] = pair;
-    row0[0] = 2 * rt * kBM + kBM;  // the later (heavier) row tile first
-    row0[1] = 2 * rt * kBM;
-  }
-  const int g = head[0] / G;
-  const int diag = Lk - Lq;  // query i sees keys <= diag + i
-  int n_tiles[kTiles];
-#pragma unroll
-  for (int t = 0; t < kTiles; ++t) {
-    if (row0[t] >= Lq) {
-      n_tiles[t] = 0;
-    } else {
-      const int kv_end = diag + min(Lq, row0[t] + kBM);  // keys this tile needs (<= Lk)
-      n_tiles[t] = (kv_end + kBN - 1) / kBN;
-    }
-  }
-  const int n_max = max(n_tiles[0], n_tiles[1]);
-  if (n_max == 0) return;
-  // With a sliding window query i sees keys >= diag + i - window + 1: the KV
-  // tiles before the one that holds the earliest such key of this CTA's rows
-  // are skipped. Steps jj = 0 .. n_steps - 1 cover KV tiles j_start + jj;
-  // stages and barrier phases count steps.
-  int j_start = 0;
-  if constexpr (kWindowed) {
-    int lo = Lk;
-#pragma unroll
-    for (int t = 0; t < kTiles; ++t)
-      if (n_tiles[t] > 0) lo = min(lo, max(0, diag + row0[t] - p.window + 1));
-    j_start = lo / kBN;
-  }
-  const int n_steps = n_max - j_start;
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + kQOff, sK = sbase + kKOff, sV = sbase + kVOff;
@@ -177,18 +234,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(bar(kBarQ), 1);
-    mbar_init(bar(kBarVTail), 1);
+    mbar_init(bar(kBarQEmpty), 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(kBarKFull + i), 1);
       mbar_init(bar(kBarVFull + i), 1);
       mbar_init(bar(kBarKEmpty + i), 1);
       mbar_init(bar(kBarVEmpty + i), 1);
+      mbar_init(bar(kBarVTail + i), 1);
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(bar(kBarS + t), 1);
       mbar_init(bar(kBarP + t), kBM);
       mbar_init(bar(kBarO + t), 1);
     }
+    mbar_init(bar(kBarDone), 1);
     *abort = 0;
     fence_barrier_init();
   }
@@ -196,124 +255,170 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(sbase + kTmemSlotOff, kTmemCols);
     tmem_relinquish();
   }
+  griddep_wait();  // inputs written by the previous kernel are visible from here on
   tc_fence_before();
-  __syncthreads();
+  // a CTA gave up waiting (in this or an earlier launch): skip the work until
+  // the error word is read and cleared; decided once per CTA
+  const bool skipped = __syncthreads_or(
+      tid == 0 && (*reinterpret_cast<volatile uint32_t *>(&g_prefill_errors) & kErrTimeout));
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kTmemSlotOff);
+  auto wait_ = [&](uint32_t b, uint32_t parity) {
+    return mbar_wait(b, parity, &g_prefill_errors, abort);
+  };
+  auto fail = [&]() {
+    *abort = 1;
+    atomicOr(&g_prefill_errors, kErrTimeout);
+  };
 
   if (warp >= kProducerWarp) {
-    setmaxnreg_dec<kOtherRegs>();
-    if (warp == kProducerWarp) {
+    setmaxnreg_dec<RegSplit<kPersistent>::kOther>();
+    if (warp == kProducerWarp && !skipped) {
       // ------------------------------------------------------------ TMA producer
-      // Lane b < kBN / box_rows owns the b-th box of every KV tile: it reads
-      // that box's block-table entry one tile ahead (the read overlaps the
-      // wait for a free stage) and issues the box's copies; lane 0 arms the
-      // barriers. K and V stages are released separately: K(j) once every
-      // S = Q K(j)^T is done, V(j) once every P.V(j) is.
+      // Per item: both Q tiles (once the previous item's S MMAs are done with
+      // the Q buffer), then K and V tiles of 128 keys. Lane b < kBN / box_rows
+      // owns the b-th box of every KV tile: it reads that box's block-table
+      // entry one tile ahead (the read overlaps the wait for a free stage) and
+      // issues the box's copies; lane 0 arms the barriers. K and V stages are
+      // released separately: K(j) once every S = Q K(j)^T is done, V(j) once
+      // every P.V(j) is.
       const int box_rows = p.box_rows;
       const int n_boxes = kBN / box_rows;
       if (lane == 0) {
         prefetch_tensormap(&q_map);
         prefetch_tensormap(&k_map);
         prefetch_tensormap(&v_map);
-        uint32_t qbytes = 0;
-#pragma unroll
-        for (int t = 0; t < kTiles; ++t) qbytes += n_tiles[t] > 0 ? kTileBytes : 0;
-        mbar_arrive_expect_tx(bar(kBarQ), qbytes);
-#pragma unroll
-        for (int t = 0; t < kTiles; ++t) {
-          if (n_tiles[t] == 0) continue;
-          tma_load_3d(sQ + t * kTileBytes, &q_map, bar(kBarQ), 0, head[t], q0 + row0[t]);
-          tma_load_3d(sQ + t * kTileBytes + kHalfBytes, &q_map, bar(kBarQ), 64, head[t],
-                      q0 + row0[t]);
-        }
       }
-      const int32_t *table = p.block_tables + static_cast<int64_t>(s) * p.max_blocks;
-      auto box_key = [&](int j) { return j * kBN + lane * box_rows; };
-      auto has_box = [&](int j) { return lane < n_boxes && j < n_max && box_key(j) < Lk; };
-      int32_t next_blk = has_box(j_start) ? __ldg(table + box_key(j_start) / p.block_size) : -1;
+      ItemWalk<kWindowed, kPersistent> w;
+      int G0 = 0;  // KV steps of earlier items
       bool good = true;
-      for (int jj = 0; jj < n_steps; ++jj) {
-        const int j = j_start + jj;
-        const int st = jj & 1;
-        const int32_t blk = next_blk;
-        if (has_box(j + 1)) next_blk = __ldg(table + box_key(j + 1) / p.block_size);
-        int32_t row = -1;
-        if (has_box(j)) {
-          if (blk < 0 || blk >= p.num_blocks)
-            atomicOr(&g_prefill_errors, kErrBlock);
-          else
-            row = blk * p.block_size + box_key(j) % p.block_size;
-        }
-        const uint32_t bytes =
-            __popc(__ballot_sync(0xffffffffu, row >= 0)) * 2u * box_rows * 128u;
-        if (jj >= kStages &&
-            !__all_sync(0xffffffffu, wait_(bar(kBarKEmpty + st), ((jj >> 1) - 1) & 1, abort))) {
+      Item it;
+      while (w.next(p, lane == 0, it)) {
+        if (w.item_no >= 1 &&
+            !__all_sync(0xffffffffu, wait_(bar(kBarQEmpty), (w.item_no - 1) & 1))) {
           good = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull + st), bytes);
-        __syncwarp();
-        const uint32_t kdst = sK + st * kTileBytes + lane * box_rows * 128;
-        if (row >= 0) {
-          tma_load_3d(kdst, &k_map, bar(kBarKFull + st), 0, g, row);
-          tma_load_3d(kdst + kHalfBytes, &k_map, bar(kBarKFull + st), 64, g, row);
+        if (lane == 0) {
+          if constexpr (kPersistent) {
+            volatile int *dv = reinterpret_cast<volatile int *>(smem + kItemOff);
+            dv[0] = it.n_tiles[0] > 0 ? it.n_tiles[0] - it.j_start : 0;
+            dv[1] = it.n_tiles[1] > 0 ? it.n_tiles[1] - it.j_start : 0;
+            dv[2] = it.n_steps;
+            dv[3] = it.Lk - (it.j_start + it.n_steps - 1) * kBN < kBN ? 1 : 0;
+          }
+          uint32_t qbytes = 0;
+#pragma unroll
+          for (int t = 0; t < kTiles; ++t) qbytes += it.n_tiles[t] > 0 ? kTileBytes : 0;
+          // the arrival releases the descriptor written above to the MMA issuer
+          mbar_arrive_expect_tx(bar(kBarQ), qbytes);
+#pragma unroll
+          for (int t = 0; t < kTiles; ++t) {
+            if (it.n_tiles[t] == 0) continue;
+            tma_load_3d(sQ + t * kTileBytes, &q_map, bar(kBarQ), 0, it.head[t],
+                        it.q0 + it.row0[t]);
+            tma_load_3d(sQ + t * kTileBytes + kHalfBytes, &q_map, bar(kBarQ), 64, it.head[t],
+                        it.q0 + it.row0[t]);
+          }
         }
-        if (jj >= kStages &&
-            !__all_sync(0xffffffffu, wait_(bar(kBarVEmpty + st), ((jj >> 1) - 1) & 1, abort))) {
-          good = false;
-          break;
+        const int n_max = it.j_start + it.n_steps;
+        const int32_t *table = p.block_tables + static_cast<int64_t>(it.s) * p.max_blocks;
+        auto box_key = [&](int j) { return j * kBN + lane * box_rows; };
+        auto has_box = [&](int j) { return lane < n_boxes && j < n_max && box_key(j) < it.Lk; };
+        int32_t next_blk =
+            has_box(it.j_start) ? __ldg(table + box_key(it.j_start) / p.block_size) : -1;
+        for (int jj = 0; jj < it.n_steps; ++jj) {
+          const int j = it.j_start + jj, gk = G0 + jj;
+          const int st = gk & 1;
+          const int32_t blk = next_blk;
+          if (has_box(j + 1)) next_blk = __ldg(table + box_key(j + 1) / p.block_size);
+          int32_t row = -1;
+          if (has_box(j)) {
+            if (blk < 0 || blk >= p.num_blocks)
+              atomicOr(&g_prefill_errors, kErrBlock);
+            else
+              row = blk * p.block_size + box_key(j) % p.block_size;
+          }
+          const uint32_t bytes =
+              __popc(__ballot_sync(0xffffffffu, row >= 0)) * 2u * box_rows * 128u;
+          if (gk >= kStages &&
+              !__all_sync(0xffffffffu, wait_(bar(kBarKEmpty + st), ((gk >> 1) - 1) & 1))) {
+            good = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull + st), bytes);
+          __syncwarp();
+          const uint32_t kdst = sK + st * kTileBytes + lane * box_rows * 128;
+          if (row >= 0) {
+            tma_load_3d(kdst, &k_map, bar(kBarKFull + st), 0, it.g, row);
+            tma_load_3d(kdst + kHalfBytes, &k_map, bar(kBarKFull + st), 64, it.g, row);
+          }
+          if (gk >= kStages &&
+              !__all_sync(0xffffffffu, wait_(bar(kBarVEmpty + st), ((gk >> 1) - 1) & 1))) {
+            good = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(bar(kBarVFull + st), bytes);
+          __syncwarp();
+          const uint32_t vdst = sV + st * kTileBytes + lane * box_rows * 128;
+          if (row >= 0) {
+            tma_load_3d(vdst, &v_map, bar(kBarVFull + st), 0, it.g, row);
+            tma_load_3d(vdst + kHalfBytes, &v_map, bar(kBarVFull + st), 64, it.g, row);
+          }
         }
-        if (lane == 0) mbar_arrive_expect_tx(bar(kBarVFull + st), bytes);
-        __syncwarp();
-        const uint32_t vdst = sV + st * kTileBytes + lane * box_rows * 128;
-        if (row >= 0) {
-          tma_load_3d(vdst, &v_map, bar(kBarVFull + st), 0, g, row);
-          tma_load_3d(vdst + kHalfBytes, &v_map, bar(kBarVFull + st), 64, g, row);
-        }
-      }
-      // every copy of this CTA is issued: the next kernel may start launching
-      if (lane == 0) griddep_launch_dependents();
-      // V rows of the last tile past the segment's last key (poison in a
-      // partly used box, stale data in boxes not loaded) are zeroed once the
-      // tile has landed, so that they never meet a zero probability
-      const int tail_r0 = Lk - (n_max - 1) * kBN;
-      if (good && tail_r0 < kBN) {
-        const int st = (n_steps - 1) & 1;
-        good = __all_sync(0xffffffffu, wait_(bar(kBarVFull + st), ((n_steps - 1) >> 1) & 1, abort));
-        if (good) {
+        if (!good) break;
+        // V rows of the item's last tile past the segment's last key (poison
+        // in a partly used box, stale data in boxes not loaded) are zeroed once
+        // the tile has landed, so that they never meet a zero probability
+        const int tail_r0 = it.Lk - (n_max - 1) * kBN;
+        if (tail_r0 < kBN) {
+          const int gk = G0 + it.n_steps - 1, st = gk & 1;
+          if (!__all_sync(0xffffffffu, wait_(bar(kBarVFull + st), (gk >> 1) & 1))) {
+            good = false;
+            break;
+          }
           const uint32_t vbase = sV + st * kTileBytes;
           const int n16 = (kBN - tail_r0) * 16;  // 16-byte pieces over both column halves
           for (int idx = lane; idx < n16; idx += 32) {
-            const int row = tail_r0 + idx / 16, piece = idx % 16;
-            const uint32_t addr = vbase + (piece / 8) * kHalfBytes + row * 128 + (piece % 8) * 16;
+            const int r = tail_r0 + idx / 16, piece = idx % 16;
+            const uint32_t addr = vbase + (piece / 8) * kHalfBytes + r * 128 + (piece % 8) * 16;
             asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(0u), "r"(0u),
                          "r"(0u), "r"(0u)
                          : "memory");
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarVTail));
+          if (lane == 0) mbar_arrive(bar(kBarVTail + st));
+        }
+        G0 += it.n_steps;
+      }
+      // every copy of this CTA is issued: the next kernel may start launching
+      if (lane == 0) griddep_launch_dependents();
+      if constexpr (kPersistent) {
+        // an empty descriptor ends the MMA issuer's walk (once it is done with
+        // the last item's descriptor: its S MMAs have completed)
+        if (good && w.item_no >= 0 &&
+            !__all_sync(0xffffffffu, wait_(bar(kBarQEmpty), w.item_no & 1)))
+          good = false;
+        if (good && lane == 0) {
+          reinterpret_cast<volatile int *>(smem + kItemOff)[2] = 0;  // n_steps
+          mbar_arrive(bar(kBarQ));
         }
       }
       // wait for the last release of each stage, so that no arrival from the
       // tensor core reaches this CTA's shared memory after it has exited
-      for (int jj = max(n_steps - kStages, 0); good && jj < n_steps; ++jj) {
-        const uint32_t par = (jj >> 1) & 1;
-        good = __all_sync(0xffffffffu, wait_(bar(kBarKEmpty + (jj & 1)), par, abort) &&
-                                           wait_(bar(kBarVEmpty + (jj & 1)), par, abort));
+      for (int gk = max(G0 - kStages, 0); good && gk < G0; ++gk) {
+        const uint32_t par = (gk >> 1) & 1;
+        good = __all_sync(0xffffffffu, wait_(bar(kBarKEmpty + (gk & 1)), par) &&
+                                           wait_(bar(kBarVEmpty + (gk & 1)), par));
       }
-      if (!good && lane == 0) fail(abort);
-    } else if (warp == kMmaWarp && lane == 0) {
+      if (!good && lane == 0) fail();
+    } else if (warp == kMmaWarp && lane == 0 && !skipped) {
       // ------------------------------------------------------------ MMA issuer
       // One thread issues every MMA and commit. K, V and Q arrive by TMA (the
       // barrier's completion orders them before the MMAs); P is written by
       // other threads' tcgen05.st, so its wait is followed by the tcgen05
       // fence that pairs with theirs.
-      // Steps are counted from the CTA's first KV tile (j_start); query tile t
-      // has steps 0 .. n_tiles[t] - j_start - 1 (none if that is not positive).
-      bool good = wait_(bar(kBarQ), 0, abort);
-      int v_ready = -1;  // last step whose V is resident (and tail-zeroed)
       // This thread shares its SM sub-partition with two softmax warps, which
       // take most issue slots while they run: every instruction here delays
       // the next MMA. So the operand descriptors are built once, as 32-bit
@@ -329,239 +434,323 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t k_lo1 = lo(smem_desc_sw128(sK + kTileBytes, 16, 1024));
       const uint32_t v_lo0 = lo(smem_desc_sw128(sV, kHalfBytes, 1024));
       const uint32_t v_lo1 = lo(smem_desc_sw128(sV + kTileBytes, kHalfBytes, 1024));
-      auto issue_s = [&](int t, int jj) -> bool {
-        const int st = jj & 1;
-        if (!wait_(bar(kBarKFull + st), (jj >> 1) & 1, abort)) return false;
-        const uint32_t tS = tmem + t * kBN;
-        const uint32_t qd = t ? q_lo1 : q_lo0;
-        const uint32_t kd = st ? k_lo1 : k_lo0;
+      uint32_t tail_parity = 0;  // bit st: parity of the next tail of V stage st
+      // The MMAs of one item: tiles 0 and 1 take n_t0 and n_t1 of its n_steps
+      // KV steps; G0, T00 and T01 count the CTA's steps (of the KV stream and
+      // of each tile) before it. Without persistence they are all 0.
+      auto run_item = [&](int n_t0, int n_t1, int n_steps, bool has_tail, int G0, int T00,
+                          int T01) -> bool {
+        int s_left = n_t0 + n_t1;  // S MMA groups of this item still to issue
+        int v_ready = -1;          // last step whose V is resident (and tail-zeroed)
+        auto issue_s = [&](int t, int jj) -> bool {
+          const int gk = G0 + jj, st = gk & 1;
+          if (!wait_(bar(kBarKFull + st), (gk >> 1) & 1)) return false;
+          const uint32_t tS = tmem + t * kBN;
+          const uint32_t qd = t ? q_lo1 : q_lo0;
+          const uint32_t kd = st ? k_lo1 : k_lo0;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off16 = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-          mma_bf16_ss(tS, qd + off16, kd + off16, desc_hi, kIdescQK, kk > 0);
-        }
-        mma_commit(bar(kBarS + t));
-        return true;
-      };
-      auto issue_pv = [&](int t, int jj) -> bool {
-        const int st = jj & 1;
-        if (v_ready != jj) {
-          // the producer zeroes the tail of the segment's last KV tile
-          const bool tail = Lk - (j_start + jj) * kBN < kBN;
-          if (!(tail ? wait_(bar(kBarVTail), 0, abort)
-                     : wait_(bar(kBarVFull + st), (jj >> 1) & 1, abort)))
-            return false;
-          v_ready = jj;
-        }
-        // P_t of this step is in TMEM once the softmax of tile t has arrived
-        if (!wait_(bar(kBarP + t), jj & 1, abort)) return false;
-        tc_fence_after();
-        const uint32_t tP = tmem + t * kBN;             // P over the first 64 columns of S_t
-        const uint32_t tO = tmem + 2 * kBN + t * kD;
-        const uint32_t vd = st ? v_lo1 : v_lo0;
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off16 = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+            mma_bf16_ss(tS, qd + off16, kd + off16, desc_hi, kIdescQK, kk > 0);
+          }
+          mma_commit(bar(kBarS + t));
+          // the item's last S: the Q buffer is free for the next item once it completes
+          if (kPersistent && --s_left == 0) mma_commit(bar(kBarQEmpty));
+          return true;
+        };
+        auto issue_pv = [&](int t, int jj) -> bool {
+          const int gk = G0 + jj, st = gk & 1;
+          if (v_ready != jj) {
+            // the producer zeroes the tail of the item's last KV tile
+            bool ok;
+            if (has_tail && jj == n_steps - 1) {
+              const uint32_t par = (tail_parity >> st) & 1u;
+              tail_parity ^= 1u << st;
+              ok = wait_(bar(kBarVTail + st), par);
+            } else {
+              ok = wait_(bar(kBarVFull + st), (gk >> 1) & 1);
+            }
+            if (!ok) return false;
+            v_ready = jj;
+          }
+          // P_t of this step is in TMEM once the softmax of tile t has arrived
+          if (!wait_(bar(kBarP + t), ((t ? T01 : T00) + jj) & 1)) return false;
+          tc_fence_after();
+          const uint32_t tP = tmem + t * kBN;             // P over the first 64 columns of S_t
+          const uint32_t tO = tmem + 2 * kBN + t * kD;
+          const uint32_t vd = st ? v_lo1 : v_lo0;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_bf16_ts(tO, tP + kk * 8, vd + ((kk * 16 * 128) >> 4), desc_hi, kIdescPV,
-                      (jj > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(kBarO + t));
-        return true;
-      };
-      for (int t = 0; good && t < kTiles; ++t)
-        if (n_tiles[t] - j_start > 0) good = issue_s(t, 0);
-      if (good) mma_commit(bar(kBarKEmpty));  // K of step 0 is free once those are done
-      for (int jj = 1; good && jj <= n_steps; ++jj) {
-        // finish step jj-1 for every query tile, starting step jj where needed
-        for (int t = 0; good && t < kTiles; ++t) {
-          if (jj - 1 >= n_tiles[t] - j_start) continue;
-          good = issue_pv(t, jj - 1);
-          if (good && jj < n_tiles[t] - j_start) good = issue_s(t, jj);
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_bf16_ts(tO, tP + kk * 8, vd + ((kk * 16 * 128) >> 4), desc_hi, kIdescPV,
+                        (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(kBarO + t));
+          return true;
+        };
+        bool ok = true;
+        if (ok && n_t0 > 0) ok = issue_s(0, 0);
+        if (ok && n_t1 > 0) ok = issue_s(1, 0);
+        if (ok) mma_commit(bar(kBarKEmpty + (G0 & 1)));  // K of step 0 is free once those are done
+        for (int jj = 1; ok && jj <= n_steps; ++jj) {
+          // finish step jj-1 for every query tile, starting step jj where needed
+          if (jj - 1 < n_t0) {
+            ok = issue_pv(0, jj - 1);
+            if (ok && jj < n_t0) ok = issue_s(0, jj);
+          }
+          if (ok && jj - 1 < n_t1) {
+            ok = issue_pv(1, jj - 1);
+            if (ok && jj < n_t1) ok = issue_s(1, jj);
+          }
+          // V of step jj-1 has had its last P.V; K of step jj its last S
+          if (ok) {
+            mma_commit(bar(kBarVEmpty + ((G0 + jj - 1) & 1)));
+            if (jj < n_steps) mma_commit(bar(kBarKEmpty + ((G0 + jj) & 1)));
+          }
         }
-        // V of step jj-1 has had its last P.V; K of step jj its last S
-        if (good) {
-          mma_commit(bar(kBarVEmpty + ((jj - 1) & 1)));
-          if (jj < n_steps) mma_commit(bar(kBarKEmpty + (jj & 1)));
+        return ok;
+      };
+      bool good = true;
+      if constexpr (kPersistent) {
+        // item by item, as the producer publishes them with their Q
+        int G0 = 0, T00 = 0, T01 = 0;
+        for (int item_no = 0; good; ++item_no) {
+          if (!wait_(bar(kBarQ), item_no & 1)) {
+            good = false;
+            break;
+          }
+          const volatile int *dv = reinterpret_cast<volatile int *>(smem + kItemOff);
+          const int n_t0 = dv[0], n_t1 = dv[1], n_steps = dv[2], tail = dv[3];
+          if (n_steps == 0) break;  // no more items
+          good = run_item(n_t0, n_t1, n_steps, tail != 0, G0, T00, T01);
+          G0 += n_steps;
+          T00 += n_t0;
+          T01 += n_t1;
+        }
+      } else {
+        Item it;
+        if (make_item<kWindowed>(p, static_cast<int>(blockIdx.x), false, it)) {
+          const int n_t0 = it.n_tiles[0] > 0 ? it.n_tiles[0] - it.j_start : 0;
+          const int n_t1 = it.n_tiles[1] > 0 ? it.n_tiles[1] - it.j_start : 0;
+          const bool tail = it.Lk - (it.j_start + it.n_steps - 1) * kBN < kBN;
+          good = wait_(bar(kBarQ), 0) && run_item(n_t0, n_t1, it.n_steps, tail, 0, 0, 0);
         }
       }
-      if (!good) fail(abort);
+      // every MMA issued here has completed before the CTA frees its TMEM
+      // (one CTA per item: the softmax warps' waits for the last P.V of each
+      // tile, which follows every other MMA, already ensure it)
+      if (kPersistent) {
+        mma_commit(bar(kBarDone));
+        if (!wait_(bar(kBarDone), 0)) good = false;
+      }
+      if (!good) fail();
     }
   } else {
-    setmaxnreg_inc<kSoftmaxRegs>();
-    // ------------------------------------------------------------ softmax / epilogue
-    const int t = warp >> 2;                // query tile of this warpgroup
-    const int quad = warp & 3;              // TMEM lane quadrant this warp may access
-    const int r = quad * 32 + lane;         // row within the tile == TMEM lane
-    const int n_t = n_tiles[t] > 0 ? n_tiles[t] - j_start : 0;  // steps of this tile
-    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tS = tmem + t * kBN + lane_off;
-    const uint32_t tO = tmem + 2 * kBN + t * kD + lane_off;
-    const int qi = row0[t] + r;             // query index within the segment
-    const int lim = diag + qi;              // last key this row may see
-    const int first = kWindowed ? lim - p.window + 1 : 0;  // first key (may be < 0)
-    // the largest first key of the tile's rows: KV tiles below it need masking
-    const int first_hi = kWindowed ? diag + row0[t] + kBM - p.window : 0;
-    // Running maximum m (log2 units) and two running sums: l of the fp32
-    // probabilities, for the lse, and lr of the same probabilities rounded to
-    // bf16 as the P.V product sees them, which normalises the output. The
-    // maximum is lazy: a row keeps its m while a tile's probabilities sum to
-    // at most 2^kLazyMax, so no probability exceeds that bound and O is
-    // rescaled only when some row of the warp passes it. Dividing by
-    // the sum of the rounded probabilities keeps the output a convex
-    // combination of the V rows with the weights the tensor core used, so a
-    // large probability rounded to bf16 costs no more than it does under an
-    // exact maximum. A row whose first tiles lie wholly before its window
-    // starts from a finite floor, so that its masked logits give probability
-    // 0 and its first visible tile rescales an O of zeros.
-    constexpr float kFloor = -1e30f;
-    float m = kFloor, l = 0.f, lr = 0.f;
-    bool good = true;
-    const uint64_t scl = f32x2(p.scale_log2, p.scale_log2);
-    for (int jj = 0; jj < n_t; ++jj) {
-      if (!__all_sync(0xffffffffu, wait_(bar(kBarS + t), jj & 1, abort))) {
-        good = false;
-        break;
-      }
-      tc_fence_after();
-      const int kbase = (j_start + jj) * kBN;
-      uint32_t x[kBN];
+    setmaxnreg_inc<RegSplit<kPersistent>::kSoftmax>();
+    if (!skipped) {
+      // ------------------------------------------------------------ softmax / epilogue
+      const int t = warp >> 2;                // query tile of this warpgroup
+      const int quad = warp & 3;              // TMEM lane quadrant this warp may access
+      const int r = quad * 32 + lane;         // row within the tile == TMEM lane
+      const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+      const uint32_t tS = tmem + t * kBN + lane_off;
+      const uint32_t tO = tmem + 2 * kBN + t * kD + lane_off;
+      const uint64_t scl = f32x2(p.scale_log2, p.scale_log2);
+      // One item's softmax and epilogue for this tile; T0 counts the tile's
+      // steps before it (0 without persistence). False if a wait gave up.
+      auto run_item = [&](const Item &it, int T0) -> bool {
+        bool good = true;
+        // this tile's part of the item, in scalars (selects, not indexed arrays)
+        const int j_start = it.j_start, Lk = it.Lk, Lq = it.Lq, diag = it.diag, q0 = it.q0;
+        const int tiles_t = t ? it.n_tiles[1] : it.n_tiles[0];
+        const int n_t = tiles_t > 0 ? tiles_t - j_start : 0;  // steps of this tile
+        const int row0 = t ? it.row0[1] : it.row0[0];
+        const int head_t = t ? it.head[1] : it.head[0];
+        const int qi = row0 + r;                // query index within the segment
+        const int lim = diag + qi;              // last key this row may see
+        const int first = kWindowed ? lim - p.window + 1 : 0;  // first key (may be < 0)
+        // the largest first key of the tile's rows: KV tiles below it need masking
+        const int first_hi = kWindowed ? diag + row0 + kBM - p.window : 0;
+        // Running maximum m (log2 units) and two running sums: l of the fp32
+        // probabilities, for the lse, and lr of the same probabilities rounded to
+        // bf16 as the P.V product sees them, which normalises the output. The
+        // maximum is lazy: a row keeps its m while a tile's probabilities sum to
+        // at most 2^kLazyMax, so no probability exceeds that bound and O is
+        // rescaled only when some row of the warp passes it. Dividing by
+        // the sum of the rounded probabilities keeps the output a convex
+        // combination of the V rows with the weights the tensor core used, so a
+        // large probability rounded to bf16 costs no more than it does under an
+        // exact maximum. A row whose first tiles lie wholly before its window
+        // starts from a finite floor, so that its masked logits give probability
+        // 0 and its first visible tile rescales an O of zeros.
+        constexpr float kFloor = -1e30f;
+        float m = kFloor, l = 0.f, lr = 0.f;
+        for (int jj = 0; jj < n_t; ++jj) {
+          if (!__all_sync(0xffffffffu, wait_(bar(kBarS + t), (T0 + jj) & 1))) {
+            good = false;
+            break;
+          }
+          tc_fence_after();
+          const int kbase = (j_start + jj) * kBN;
+          uint32_t x[kBN];
 #pragma unroll
-      for (int c = 0; c < kBN; c += 32)
-        tmem_ld32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(&x[c]));
-      tmem_wait_ld();
-      // keys past the row's causal limit or the segment end, or before its
-      // window, are masked (their logit becomes -inf, their probability 0);
-      // only the diagonal, the tail and the window's first tiles have any
-      if ((kbase + kBN - 1 > diag + row0[t]) || (kbase + kBN > Lk) ||
-          (kWindowed && kbase < first_hi)) {
-        const int keep = min(lim, Lk - 1) - kbase + 1;  // columns < keep are at or before the limit
-        if constexpr (kWindowed) {
-          const int skip = first - kbase;               // columns < skip are before the window
+          for (int c = 0; c < kBN; c += 32)
+            tmem_ld32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(&x[c]));
+          tmem_wait_ld();
+          // keys past the row's causal limit or the segment end, or before its
+          // window, are masked (their logit becomes -inf, their probability 0);
+          // only the diagonal, the tail and the window's first tiles have any
+          if ((kbase + kBN - 1 > diag + row0) || (kbase + kBN > Lk) ||
+              (kWindowed && kbase < first_hi)) {
+            const int keep = min(lim, Lk - 1) - kbase + 1;  // columns < keep: at or before the limit
+            if constexpr (kWindowed) {
+              const int skip = first - kbase;                  // columns < skip: before the window
 #pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (c >= keep || c < skip) x[c] = 0xFF800000u;
-        } else {
-#pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (c >= keep) x[c] = 0xFF800000u;
-        }
-      }
-      // P = 2^(x * scale - mm), packed two per column over the first 64
-      // columns of S_t (all of S is already in registers); ts and tr get the
-      // tile's sums of the fp32 and of the bf16-rounded probabilities
-      auto exps = [&](float mm, float &ts, float &tr) {
-        const uint64_t nm = f32x2(-mm, -mm);
-        uint64_t s0 = 0, s1 = 0;
-        float r0l = 0.f, r0h = 0.f, r1l = 0.f, r1h = 0.f;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int k = hf * 64 + 2 * c;
-            const uint64_t e =
-                fma2(f32x2(__uint_as_float(x[k]), __uint_as_float(x[k + 1])), scl, nm);
-            const float p0 = fast_exp2(f32x2_lo(e)), p1 = fast_exp2(f32x2_hi(e));
-            pk[c] = pack_bf16x2(p0, p1);
-            if (c & 1) {
-              add2(s1, f32x2(p0, p1));
-              add_bf16x2_to_f32(r1l, r1h, pk[c]);
+              for (int c = 0; c < kBN; ++c)
+                if (c >= keep || c < skip) x[c] = 0xFF800000u;
             } else {
-              add2(s0, f32x2(p0, p1));
-              add_bf16x2_to_f32(r0l, r0h, pk[c]);
+#pragma unroll
+              for (int c = 0; c < kBN; ++c)
+                if (c >= keep) x[c] = 0xFF800000u;
             }
           }
-          tmem_st32(tS + hf * 32, pk);
+          // P = 2^(x * scale - mm), packed two per column over the first 64
+          // columns of S_t (all of S is already in registers); ts and tr get the
+          // tile's sums of the fp32 and of the bf16-rounded probabilities
+          auto exps = [&](float mm, float &ts, float &tr) {
+            const uint64_t nm = f32x2(-mm, -mm);
+            uint64_t s0 = 0, s1 = 0;
+            float r0l = 0.f, r0h = 0.f, r1l = 0.f, r1h = 0.f;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              uint32_t pk[32];
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const int k = hf * 64 + 2 * c;
+                const uint64_t e =
+                    fma2(f32x2(__uint_as_float(x[k]), __uint_as_float(x[k + 1])), scl, nm);
+                const float p0 = fast_exp2(f32x2_lo(e)), p1 = fast_exp2(f32x2_hi(e));
+                pk[c] = pack_bf16x2(p0, p1);
+                if (c & 1) {
+                  add2(s1, f32x2(p0, p1));
+                  add_bf16x2_to_f32(r1l, r1h, pk[c]);
+                } else {
+                  add2(s0, f32x2(p0, p1));
+                  add_bf16x2_to_f32(r0l, r0h, pk[c]);
+                }
+              }
+              tmem_st32(tS + hf * 32, pk);
+            }
+            add2(s0, s1);
+            ts = f32x2_lo(s0) + f32x2_hi(s0);
+            tr = (r0l + r1l) + (r0h + r1h);
+          };
+          // First with the row's current maximum, without looking for a larger
+          // one: if no row of the warp then has a tile sum above 2^kLazyMax, no
+          // probability exceeds that bound either and the tile is done. Otherwise
+          // (some logit lies more than a little above m; an infinite sum included)
+          // the warp takes the exact maximum, rescales O and recomputes P over
+          // what it wrote. The first tile of a row always takes the maximum.
+          float ts, tr;
+          bool exact = jj == 0;
+#pragma unroll 1
+          for (;;) {
+            if (exact) {
+              // row max of the raw logits (the scale is positive): eight chains
+              // of three-input maxima
+              float a[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(x[i]);
+#pragma unroll
+              for (int c = 8; c < kBN; c += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  a[i] = fmax3(a[i], __uint_as_float(x[c + i]), __uint_as_float(x[c + 8 + i]));
+              const float mx =
+                  fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+              const float mxs = mx * p.scale_log2;  // -inf stays -inf
+              if (jj == 0) {
+                // nothing is in O yet; without a window every row sees key 0
+                m = kWindowed ? fmaxf(mxs, kFloor) : mxs;
+              } else {
+                // P.V of the previous step is complete (this S was issued after
+                // it): rescale the O rows in TMEM. The accesses are warp-wide, so
+                // the whole warp takes its new maxima.
+                const float m_new = fmaxf(m, mxs);
+                const float alpha = fast_exp2(m - m_new);
+                // 32 columns at a time: all of S is held in registers meanwhile
+#pragma unroll 1
+                for (int c = 0; c < kD; c += 32) {
+                  uint32_t o[32];
+                  tmem_ld32(tO + c, o);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                  tmem_st32(tO + c, o);
+                }
+                tmem_wait_st();
+                l *= alpha;
+                lr *= alpha;
+                m = m_new;
+              }
+            }
+            exps(m, ts, tr);
+            if (exact || !__any_sync(0xffffffffu, !(ts <= kLazyBound))) break;
+            exact = true;
+          }
+          l += ts;
+          lr += tr;
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(kBarP + t));
         }
-        add2(s0, s1);
-        ts = f32x2_lo(s0) + f32x2_hi(s0);
-        tr = (r0l + r1l) + (r0h + r1h);
+        if (!good) return false;
+        if (n_t > 0) {
+          // epilogue: the last P.V of the item has completed once its O barrier
+          // phase has; the next item's first P.V (which overwrites O) waits for
+          // this warp's next P, written only after these reads
+          if (!__all_sync(0xffffffffu, wait_(bar(kBarO + t), (T0 + n_t - 1) & 1))) return false;
+          tc_fence_after();
+          const float inv_l = 1.f / lr;
+          const bool store = qi < Lq;
+          __nv_bfloat16 *orow =
+              p.out + (static_cast<int64_t>(q0 + qi) * p.num_q_heads + head_t) * kD;
+#pragma unroll
+          for (int c = 0; c < kD / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_wait_ld();
+            if (store) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 8) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(o[i + 0]) * inv_l, __uint_as_float(o[i + 1]) * inv_l);
+                v.y = pack_bf16x2(__uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+                v.z = pack_bf16x2(__uint_as_float(o[i + 4]) * inv_l, __uint_as_float(o[i + 5]) * inv_l);
+                v.w = pack_bf16x2(__uint_as_float(o[i + 6]) * inv_l, __uint_as_float(o[i + 7]) * inv_l);
+                *reinterpret_cast<uint4 *>(orow + c * 32 + i) = v;
+              }
+            }
+          }
+          if (store && p.lse != nullptr)
+            p.lse[static_cast<int64_t>(q0 + qi) * p.num_q_heads + head_t] =
+                (m + log2f(l)) * kLn2;
+        }
+        return true;
       };
-      // First with the row's current maximum, without looking for a larger
-      // one: if no row of the warp then has a tile sum above 2^kLazyMax, no
-      // probability exceeds that bound either and the tile is done. Otherwise
-      // (some logit lies more than a little above m; an infinite sum included)
-      // the warp takes the exact maximum, rescales O and recomputes P over
-      // what it wrote. The first tile of a row always takes the maximum.
-      float ts, tr;
-      bool exact = jj == 0;
-#pragma unroll 1
-      for (;;) {
-        if (exact) {
-          // row max of the raw logits (the scale is positive): eight chains
-          // of three-input maxima
-          float a[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(x[i]);
-#pragma unroll
-          for (int c = 8; c < kBN; c += 16)
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              a[i] = fmax3(a[i], __uint_as_float(x[c + i]), __uint_as_float(x[c + 8 + i]));
-          const float mx =
-              fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
-          const float mxs = mx * p.scale_log2;  // -inf stays -inf
-          if (jj == 0) {
-            // nothing is in O yet; without a window every row sees key 0
-            m = kWindowed ? fmaxf(mxs, kFloor) : mxs;
-          } else {
-            // P.V of the previous step is complete (this S was issued after
-            // it): rescale the O rows in TMEM. The accesses are warp-wide, so
-            // the whole warp takes its new maxima.
-            const float m_new = fmaxf(m, mxs);
-            const float alpha = fast_exp2(m - m_new);
-            // 32 columns at a time: all of S is held in registers meanwhile
-#pragma unroll 1
-            for (int c = 0; c < kD; c += 32) {
-              uint32_t o[32];
-              tmem_ld32(tO + c, o);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st32(tO + c, o);
-            }
-            tmem_wait_st();
-            l *= alpha;
-            lr *= alpha;
-            m = m_new;
-          }
+      bool good = true;
+      if constexpr (kPersistent) {
+        ItemWalk<kWindowed, kPersistent> w;
+        int T0 = 0;  // steps of this tile in earlier items
+        Item it;
+        while (good && w.next(p, false, it)) {
+          good = run_item(it, T0);
+          const int tiles_t = t ? it.n_tiles[1] : it.n_tiles[0];
+          T0 += tiles_t > 0 ? tiles_t - it.j_start : 0;
         }
-        exps(m, ts, tr);
-        if (exact || !__any_sync(0xffffffffu, !(ts <= kLazyBound))) break;
-        exact = true;
+      } else {
+        Item it;
+        if (make_item<kWindowed>(p, static_cast<int>(blockIdx.x), false, it)) good = run_item(it, 0);
       }
-      l += ts;
-      lr += tr;
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(kBarP + t));
-    }
-    if (n_t > 0 &&
-        __all_sync(0xffffffffu, good && wait_(bar(kBarO + t), (n_t - 1) & 1, abort))) {
-      tc_fence_after();
-      const float inv_l = 1.f / lr;
-      const bool store = qi < Lq;
-      __nv_bfloat16 *orow =
-          p.out + (static_cast<int64_t>(q0 + qi) * p.num_q_heads + head[t]) * kD;
-#pragma unroll
-      for (int c = 0; c < kD / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + c * 32, o);
-        tmem_wait_ld();
-        if (store) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[i + 0]) * inv_l, __uint_as_float(o[i + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(o[i + 4]) * inv_l, __uint_as_float(o[i + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(o[i + 6]) * inv_l, __uint_as_float(o[i + 7]) * inv_l);
-            *reinterpret_cast<uint4 *>(orow + c * 32 + i) = v;
-          }
-        }
-      }
-      if (store && p.lse != nullptr)
-        p.lse[static_cast<int64_t>(q0 + qi) * p.num_q_heads + head[t]] = (m + log2f(l)) * kLn2;
-    } else if (n_t > 0 && r == 0) {
-      fail(abort);
+      if (!good && r == 0) fail();
     }
   }
 
@@ -575,23 +764,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <bool kWindowed>
+template <bool kWindowed, bool kPersistent>
 cudaError_t launch_instance(dim3 grid, const CUtensorMap &q_map, const CUtensorMap &k_map,
                             const CUtensorMap &v_map, const PrefillParams &p,
                             cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kWindowed>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  auto kern = prefill_kernel<kWindowed, kPersistent>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   // setmaxnreg.inc waits until registers released by the other warpgroup are
   // free: launch only a build whose per-thread allocation covers the split
   static const int launch_regs = [] {
     cudaFuncAttributes fa{};
-    return cudaFuncGetAttributes(&fa, prefill_kernel<kWindowed>) == cudaSuccess ? fa.numRegs : 0;
+    return cudaFuncGetAttributes(&fa, prefill_kernel<kWindowed, kPersistent>) == cudaSuccess
+               ? fa.numRegs
+               : 0;
   }();
-  if (launch_regs * kThreads < (2 * kSoftmaxRegs + kOtherRegs) * 128)
+  using R = RegSplit<kPersistent>;
+  if (launch_regs * kThreads < (2 * R::kSoftmax + R::kOther) * 128)
     return cudaErrorInvalidConfiguration;
-  return launch_pdl(prefill_kernel<kWindowed>, grid, dim3(kThreads), kSmemBytes, stream, q_map,
-                    k_map, v_map, p);
+  return launch_pdl(kern, grid, dim3(kThreads), kSmemBytes, stream, q_map, k_map, v_map, p);
 }
 
 cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
@@ -614,14 +806,22 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
   p.num_kv_heads = a.num_kv_heads;
   p.block_size = a.block_size;
   p.num_blocks = a.num_blocks;
-  const int rows_per_cta = G >= 2 ? kBM : 2 * kBM;
-  p.n_rowtiles = (a.max_seqlen_q + rows_per_cta - 1) / rows_per_cta;
+  const int rows_per_item = G >= 2 ? kBM : 2 * kBM;
+  p.n_rowtiles = (a.max_seqlen_q + rows_per_item - 1) / rows_per_item;
+  p.n_pairs = G >= 2 ? a.num_q_heads / 2 : a.num_q_heads;
+  const int64_t n_items = static_cast<int64_t>(p.n_rowtiles) * p.n_pairs * a.num_seqs;
+  if (n_items > kMaxPrefillItems) return cudaErrorInvalidValue;
+  p.n_items = static_cast<int32_t>(n_items);
   p.window = a.window;
   p.box_rows = a.box_rows;
   p.scale_log2 = a.scale_log2;
-  dim3 grid(p.n_rowtiles, G >= 2 ? a.num_q_heads / 2 : a.num_q_heads, a.num_seqs);
-  return p.window > 0 ? launch_instance<true>(grid, q_map, k_map, v_map, p, stream)
-                      : launch_instance<false>(grid, q_map, k_map, v_map, p, stream);
+  if (p.window > 0) {
+    // persistent: one CTA per SM (the shared memory admits no second one)
+    const dim3 grid(static_cast<unsigned>(n_items < a.num_sms ? n_items : a.num_sms));
+    return launch_instance<true, true>(grid, q_map, k_map, v_map, p, stream);
+  }
+  return launch_instance<false, false>(dim3(static_cast<unsigned>(n_items)), q_map, k_map, v_map,
+                                       p, stream);
 }
 
 cudaError_t prefill_error_word(uint32_t **word) {
