@@ -710,40 +710,70 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
       }
       continue;
     }
+    // more pieces (long contexts cut across many CTAs): the maxima of up to
+    // 32 pieces a round, one piece per lane and every head at once; then each
+    // lane's weight and sum, and the outputs in batches of kMergeFast pieces
+    // whose loads (all heads) are issued before any is used
+    float M[G], Lsum[G], acc[G][4];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      float M = -INFINITY;
-      for (int64_t x = wa + lane; x <= wb; x += 32) M = fmaxf(M, p.ws_ml[part(x, h) * 2]);
+      M[h] = -INFINITY;
+      Lsum[h] = 0.f;
+      acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
+    }
+    for (int64_t x = wa + lane; x <= wb; x += 32)
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-      float Lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int64_t base = wa; base <= wb; base += 32) {
-        const int64_t x = base + lane;
-        float f = 0.f;
+      for (int h = 0; h < G; ++h) M[h] = fmaxf(M[h], p.ws_ml[part(x, h) * 2]);
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M[h] = fmaxf(M[h], __shfl_xor_sync(0xffffffffu, M[h], off));
+#pragma unroll 1
+    for (int64_t base = wa; base <= wb; base += 32) {
+      const int64_t x = base + lane;
+      float f[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        f[h] = 0.f;
         if (x <= wb) {
           const int64_t i = part(x, h);
-          f = fast_exp2(p.ws_ml[i * 2] - M);
-          Lsum += p.ws_ml[i * 2 + 1] * f;
-        }
-        const int n = static_cast<int>(wb - base + 1 < 32 ? wb - base + 1 : 32);
-#pragma unroll 4
-        for (int j = 0; j < n; ++j) {
-          const float fj = __shfl_sync(0xffffffffu, f, j);
-          const float4 ov = reinterpret_cast<const float4 *>(p.ws_o + part(base + j, h) * kD)[lane];
-          acc[0] = fmaf(ov.x, fj, acc[0]);
-          acc[1] = fmaf(ov.y, fj, acc[1]);
-          acc[2] = fmaf(ov.z, fj, acc[2]);
-          acc[3] = fmaf(ov.w, fj, acc[3]);
+          f[h] = fast_exp2(p.ws_ml[i * 2] - M[h]);
+          Lsum[h] += p.ws_ml[i * 2 + 1] * f[h];
         }
       }
+      const int n = static_cast<int>(wb - base + 1 < 32 ? wb - base + 1 : 32);
+#pragma unroll 1
+      for (int j0 = 0; j0 < n; j0 += kMergeFast) {
+        float4 ov[kMergeFast][G];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
-      const float inv = 1.f / Lsum;
+        for (int j = 0; j < kMergeFast; ++j)
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            ov[j][h] = j0 + j < n ? reinterpret_cast<const float4 *>(
+                                        p.ws_o + part(base + j0 + j, h) * kD)[lane]
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < kMergeFast; ++j)
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float fj = __shfl_sync(0xffffffffu, f[h], (j0 + j) & 31);
+            acc[h][0] = fmaf(ov[j][h].x, fj, acc[h][0]);
+            acc[h][1] = fmaf(ov[j][h].y, fj, acc[h][1]);
+            acc[h][2] = fmaf(ov[j][h].z, fj, acc[h][2]);
+            acc[h][3] = fmaf(ov[j][h].w, fj, acc[h][3]);
+          }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) Lsum[h] += __shfl_xor_sync(0xffffffffu, Lsum[h], off);
+      const float inv = 1.f / Lsum[h];
       uint2 v;
-      v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-      v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      v.x = pack_bf16x2(acc[h][0] * inv, acc[h][1] * inv);
+      v.y = pack_bf16x2(acc[h][2] * inv, acc[h][3] * inv);
       *reinterpret_cast<uint2 *>(p.out + (row0 + h) * kD + lane * 4) = v;
-      if (lane == 0 && p.lse != nullptr) p.lse[row0 + h] = (M + log2f(Lsum)) * kLn2;
+      if (lane == 0 && p.lse != nullptr) p.lse[row0 + h] = (M[h] + log2f(Lsum[h])) * kLn2;
     }
   }
 }
