@@ -52,10 +52,12 @@ constexpr int kRowBytes = kD * 2;       // 256 bytes of one head's K (or V) row
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kLazyMax = 8.0f;         // log2 units the running max may lag
 constexpr int kMergeFast = 8;            // pieces merged with all loads issued at once
-// warps per merge CTA: small enough for a merge CTA to fit beside a decode CTA
+// warps per merge CTA (2-warp CTAs that fit beside a decode CTA, one per SM,
+// measured slower: each warp then merges more pairs)
 constexpr int kMergeWarps = 4;
 
 struct DecodeParams {
+  const uint8_t *q;                // queries [S, H_q, D] (the CTA's first segment reads them directly)
   const uint4 *k_new, *v_new;      // fused store: the new tokens' rows [S, H_kv, D] (or null)
   uint4 *k_cache_w, *v_cache_w;    // fused store: the caches, written through these
   const int32_t *slot_mapping;     // fused store: slot of each sequence's new token
@@ -165,6 +167,9 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
                   const __grid_constant__ CUtensorMap kn_map,
                   const __grid_constant__ CUtensorMap vn_map, const DecodeParams p) {
   using L = DecodeSmem<G, kMaxHG, NS>;
+  // the consumers load the q rows of the CTA's first segment themselves (G <=
+  // 2: with four query heads a KV head the registers that takes would spill)
+  constexpr bool kDirectQ = G <= 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                               ~static_cast<uintptr_t>(127));
@@ -289,7 +294,9 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
       const int st = i % NS;
       const uint32_t stage = stage0 + st * L::kStageBytes;
       const uint32_t bar = full0 + 8 * st;
-      const bool with_q = (i == 0) || (c.k == 0);
+      // the q rows of every segment the CTA opens (with kDirectQ, after its
+      // first: those of the first the consumers load themselves)
+      const bool with_q = kDirectQ ? (i > 0 && c.k == 0) : (i == 0 || c.k == 0);
       const bool with_new = fused && c.k == chunks_of(prefix, c.s) - 1;
       const bool ok = blk >= 0 && blk < p.num_blocks;
       if (arm) {
@@ -378,6 +385,20 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
   const int half = lane >> 4, vcol = lane & 15;
   float *prob = reinterpret_cast<float *>(smem + L::kProbOffset) + g * G * kChunk;
   Cursor cur = locate(prefix, p.num_seqs, n_groups, u_lo);
+  // With kDirectQ the q rows of the CTA's first segment come straight from
+  // global memory, loaded here while the first stage lands: a TMA copy issued
+  // after the dependency wait would queue behind the K/V copies issued before
+  // it.
+  uint4 q_first[kDirectQ ? G : 1][2];
+  if constexpr (kDirectQ) {
+    const uint8_t *qg =
+        p.q + (static_cast<int64_t>(cur.s) * p.num_q_heads + (cur.hg * HG + g) * G) * kRowBytes;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      q_first[h][0] = __ldg(reinterpret_cast<const uint4 *>(qg + h * kRowBytes + sub * 16));
+      q_first[h][1] = __ldg(reinterpret_cast<const uint4 *>(qg + h * kRowBytes + 128 + sub * 16));
+    }
+  }
   uint64_t qf[G][8];  // the lane's 16 query dims per head, as scaled fp32 pairs
   float m[G], lsum[G];
   uint64_t o[G][4];   // the lane's 8 output dims per head, as fp32 pairs
@@ -404,8 +425,14 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
       const uint8_t *qs = kst + 2 * L::kKBytes + g * G * kRowBytes;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(qs + h * kRowBytes + sub * 16);
-        const uint4 b = *reinterpret_cast<const uint4 *>(qs + h * kRowBytes + 128 + sub * 16);
+        uint4 a, b;
+        if (kDirectQ && it == 0) {
+          a = q_first[kDirectQ ? h : 0][0];
+          b = q_first[kDirectQ ? h : 0][1];
+        } else {
+          a = *reinterpret_cast<const uint4 *>(qs + h * kRowBytes + sub * 16);
+          b = *reinterpret_cast<const uint4 *>(qs + h * kRowBytes + 128 + sub * 16);
+        }
         const uint32_t wq[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -820,6 +847,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &k_map,
                           const CUtensorMap &kn_map, const CUtensorMap &vn_map,
                           cudaStream_t stream) {
   DecodeParams p;
+  p.q = static_cast<const uint8_t *>(a.q);
   p.k_new = static_cast<const uint4 *>(a.k_new);
   p.v_new = static_cast<const uint4 *>(a.v_new);
   p.k_cache_w = static_cast<uint4 *>(a.k_cache_w);
