@@ -32,6 +32,14 @@
 //              end normalise O and store the bf16 output and the natural-log
 //              lse.
 // While one tile's softmax runs, the tensor pipe works on the other tile.
+//
+// Two kernels share this design. Without a sliding window, prefill_kernel
+// runs one CTA per work item (two query tiles); with one, where an item is
+// only two or three KV steps, prefill_persistent_kernel runs one CTA per SM
+// that walks its share of the items, so that the set-up, the TMEM allocation
+// and the pipeline's fill and drain are paid once per SM rather than once per
+// item. (The persistent walk measured slower on long items, so the first
+// kernel stays for them.)
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -88,6 +96,7 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, 0, 1);   // A=P (TMEM), B=
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kLazyMax = 8.0f;  // log2 units the running maximum may lag
 constexpr float kLazyBound = 256.0f;  // 2^kLazyMax: the largest tile sum taken as is
+static_assert(kLazyBound == 256.0f && kLazyMax == 8.0f, "kLazyBound is 2^kLazyMax");
 
 struct PrefillParams {
   const int32_t *cu_q, *cu_k, *block_tables;
@@ -181,8 +190,7 @@ __device__ __forceinline__ bool make_item(const PrefillParams &p, int lin, bool 
 // This CTA's items in order: CTA c of C takes items c, 2C - 1 - c, 2C + c, ...
 // of the heaviest-first list (rounds alternate direction, so that every CTA
 // gets a similar mix of heavy and light items).
-// Without persistence CTA c takes item c alone.
-template <bool kWindowed, bool kPersistent>
+template <bool kWindowed>
 struct ItemWalk {
   int k = 0;         // next round to look at
   int item_no = -1;  // index of the current item among this CTA's items with work
@@ -190,7 +198,6 @@ struct ItemWalk {
   __device__ __forceinline__ bool next(const PrefillParams &p, bool raise, Item &it) {
     const int C = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
     for (;;) {
-      if (!kPersistent && k > 0) return false;
       const int lin = k * C + ((k & 1) ? C - 1 - c : c);
       ++k;
       if (lin >= p.n_items) return false;
@@ -202,23 +209,480 @@ struct ItemWalk {
   }
 };
 
-// kWindowed: a sliding window is set (p.window > 0). The kernel without one
-// is a separate instantiation, so that it keeps no window bookkeeping at all.
-//
-// kPersistent: one CTA per SM walks its items (used with a window, where an
-// item is two or three KV steps and a CTA's fixed cost, a few microseconds of
-// set-up, pipeline fill and drain, would otherwise rival its work); else one
-// CTA per item, in the list's order (long items: the hardware's assignment of
-// CTAs to SMs as they free up balances them). Barrier phases run on across
-// items: K/V stages and the V-tail barriers count the CTA's KV steps, the S,
+// Without a sliding window: one CTA per item, CTA c taking item c of the
+// heaviest-first list (the hardware hands CTAs to SMs as they free up, which
+// balances these long items). Calls with a window run
+// prefill_persistent_kernel.
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap q_map,
+                   const __grid_constant__ CUtensorMap k_map,
+                   const __grid_constant__ CUtensorMap v_map, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // CTA -> (sequence, head pair, row tile): the heaviest row tiles (the last
+  // ones, which see the most keys) of every head pair and sequence first, the
+  // lightest last, so that the grid's tail holds the shortest CTAs.
+  // (a 3-D grid (row tiles, head pairs, sequences) where its dimensions fit,
+  // else a 1-D one: the same linear index either way; the 3-D grid's CTA
+  // order measured about 1 % faster)
+  const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  const int per_rt = p.n_pairs * p.num_seqs;  // items per row tile index
+  const int rt = p.n_rowtiles - 1 - lin / per_rt;
+  const int pair = (lin % per_rt) % p.n_pairs;
+  const int s = (lin % per_rt) / p.n_pairs;
+  const int G = p.num_q_heads / p.num_kv_heads;
+
+  griddep_wait();  // inputs written by the previous kernel are visible from here on
+  // a CTA gave up waiting (in this or an earlier launch): skip the work until
+  // the error word is read and cleared; decided once per CTA
+  if (__syncthreads_or(tid == 0 &&
+                       (*reinterpret_cast<volatile uint32_t *>(&g_prefill_errors) & kErrTimeout)))
+    return;
+
+  const int q0 = p.cu_q[s], q1 = p.cu_q[s + 1];
+  const int Lq = q1 - q0, Lk = p.cu_k[s + 1] - p.cu_k[s];
+  if (q0 < 0 || Lq < 0 || Lk < Lq || Lq > p.max_seqlen_q || Lk > p.max_seqlen_k ||
+      q1 > p.total_q ||
+      static_cast<int64_t>(Lk) > static_cast<int64_t>(p.max_blocks) * p.block_size) {
+    if (rt == p.n_rowtiles - 1 && pair == 0 && tid == 0) atomicOr(&g_prefill_errors, kErrSeqlens);
+    return;
+  }
+  // the two query tiles: (head, first row) each; heaviest row tiles first
+  int head[kTiles], row0[kTiles];
+  if (G >= 2) {
+    head[0] = 2 * pair;
+    head[1] = 2 * pair + 1;
+    row0[0] = row0[1] = rt * kBM;
+  } else {
+    head[0] = head[1] = pair;
+    row0[0] = 2 * rt * kBM + kBM;  // the later (heavier) row tile first
+    row0[1] = 2 * rt * kBM;
+  }
+  const int g = head[0] / G;
+  const int diag = Lk - Lq;  // query i sees keys <= diag + i
+  int n_tiles[kTiles];
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t) {
+    if (row0[t] >= Lq) {
+      n_tiles[t] = 0;
+    } else {
+      const int kv_end = diag + min(Lq, row0[t] + kBM);  // keys this tile needs (<= Lk)
+      n_tiles[t] = (kv_end + kBN - 1) / kBN;
+    }
+  }
+  const int n_max = max(n_tiles[0], n_tiles[1]);
+  if (n_max == 0) return;
+  // steps jj = 0 .. n_steps - 1 cover KV tiles j_start + jj (the form the
+  // persistent kernel shares, where a window may skip leading tiles)
+  const int j_start = 0;
+  const int n_steps = n_max - j_start;
+
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + kQOff, sK = sbase + kKOff, sV = sbase + kVOff;
+  const uint32_t bars = sbase + kBarOff;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  volatile int *abort = reinterpret_cast<volatile int *>(smem + kAbortOff);
+
+  if (tid == 0) {
+    mbar_init(bar(kBarQ), 1);
+    mbar_init(bar(kBarVTail), 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(bar(kBarKFull + i), 1);
+      mbar_init(bar(kBarVFull + i), 1);
+      mbar_init(bar(kBarKEmpty + i), 1);
+      mbar_init(bar(kBarVEmpty + i), 1);
+    }
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(bar(kBarS + t), 1);
+      mbar_init(bar(kBarP + t), kBM);
+      mbar_init(bar(kBarO + t), 1);
+    }
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kProducerWarp) {
+    tmem_alloc(sbase + kTmemSlotOff, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kTmemSlotOff);
+
+  if (warp >= kProducerWarp) {
+    setmaxnreg_dec<RegSplit<false>::kOther>();
+    if (warp == kProducerWarp) {
+      // ------------------------------------------------------------ TMA producer
+      // Lane b < kBN / box_rows owns the b-th box of every KV tile: it reads
+      // that box's block-table entry one tile ahead (the read overlaps the
+      // wait for a free stage) and issues the box's copies; lane 0 arms the
+      // barriers. K and V stages are released separately: K(j) once every
+      // S = Q K(j)^T is done, V(j) once every P.V(j) is.
+      const int box_rows = p.box_rows;
+      const int n_boxes = kBN / box_rows;
+      if (lane == 0) {
+        prefetch_tensormap(&q_map);
+        prefetch_tensormap(&k_map);
+        prefetch_tensormap(&v_map);
+        uint32_t qbytes = 0;
+#pragma unroll
+        for (int t = 0; t < kTiles; ++t) qbytes += n_tiles[t] > 0 ? kTileBytes : 0;
+        mbar_arrive_expect_tx(bar(kBarQ), qbytes);
+#pragma unroll
+        for (int t = 0; t < kTiles; ++t) {
+          if (n_tiles[t] == 0) continue;
+          tma_load_3d(sQ + t * kTileBytes, &q_map, bar(kBarQ), 0, head[t], q0 + row0[t]);
+          tma_load_3d(sQ + t * kTileBytes + kHalfBytes, &q_map, bar(kBarQ), 64, head[t],
+                      q0 + row0[t]);
+        }
+      }
+      const int32_t *table = p.block_tables + static_cast<int64_t>(s) * p.max_blocks;
+      auto box_key = [&](int j) { return j * kBN + lane * box_rows; };
+      auto has_box = [&](int j) { return lane < n_boxes && j < n_max && box_key(j) < Lk; };
+      int32_t next_blk = has_box(j_start) ? __ldg(table + box_key(j_start) / p.block_size) : -1;
+      bool good = true;
+      for (int jj = 0; jj < n_steps; ++jj) {
+        const int j = j_start + jj;
+        const int st = jj & 1;
+        const int32_t blk = next_blk;
+        if (has_box(j + 1)) next_blk = __ldg(table + box_key(j + 1) / p.block_size);
+        int32_t row = -1;
+        if (has_box(j)) {
+          if (blk < 0 || blk >= p.num_blocks)
+            atomicOr(&g_prefill_errors, kErrBlock);
+          else
+            row = blk * p.block_size + box_key(j) % p.block_size;
+        }
+        const uint32_t bytes =
+            __popc(__ballot_sync(0xffffffffu, row >= 0)) * 2u * box_rows * 128u;
+        if (jj >= kStages &&
+            !__all_sync(0xffffffffu, wait_(bar(kBarKEmpty + st), ((jj >> 1) - 1) & 1, abort))) {
+          good = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull + st), bytes);
+        __syncwarp();
+        const uint32_t kdst = sK + st * kTileBytes + lane * box_rows * 128;
+        if (row >= 0) {
+          tma_load_3d(kdst, &k_map, bar(kBarKFull + st), 0, g, row);
+          tma_load_3d(kdst + kHalfBytes, &k_map, bar(kBarKFull + st), 64, g, row);
+        }
+        if (jj >= kStages &&
+            !__all_sync(0xffffffffu, wait_(bar(kBarVEmpty + st), ((jj >> 1) - 1) & 1, abort))) {
+          good = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar(kBarVFull + st), bytes);
+        __syncwarp();
+        const uint32_t vdst = sV + st * kTileBytes + lane * box_rows * 128;
+        if (row >= 0) {
+          tma_load_3d(vdst, &v_map, bar(kBarVFull + st), 0, g, row);
+          tma_load_3d(vdst + kHalfBytes, &v_map, bar(kBarVFull + st), 64, g, row);
+        }
+      }
+      // every copy of this CTA is issued: the next kernel may start launching
+      if (lane == 0) griddep_launch_dependents();
+      // V rows of the last tile past the segment's last key (poison in a
+      // partly used box, stale data in boxes not loaded) are zeroed once the
+      // tile has landed, so that they never meet a zero probability
+      const int tail_r0 = Lk - (n_max - 1) * kBN;
+      if (good && tail_r0 < kBN) {
+        const int st = (n_steps - 1) & 1;
+        good = __all_sync(0xffffffffu, wait_(bar(kBarVFull + st), ((n_steps - 1) >> 1) & 1, abort));
+        if (good) {
+          const uint32_t vbase = sV + st * kTileBytes;
+          const int n16 = (kBN - tail_r0) * 16;  // 16-byte pieces over both column halves
+          for (int idx = lane; idx < n16; idx += 32) {
+            const int row = tail_r0 + idx / 16, piece = idx % 16;
+            const uint32_t addr = vbase + (piece / 8) * kHalfBytes + row * 128 + (piece % 8) * 16;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(0u), "r"(0u),
+                         "r"(0u), "r"(0u)
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarVTail));
+        }
+      }
+      // wait for the last release of each stage, so that no arrival from the
+      // tensor core reaches this CTA's shared memory after it has exited
+      for (int jj = max(n_steps - kStages, 0); good && jj < n_steps; ++jj) {
+        const uint32_t par = (jj >> 1) & 1;
+        good = __all_sync(0xffffffffu, wait_(bar(kBarKEmpty + (jj & 1)), par, abort) &&
+                                           wait_(bar(kBarVEmpty + (jj & 1)), par, abort));
+      }
+      if (!good && lane == 0) fail(abort);
+    } else if (warp == kMmaWarp && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      // One thread issues every MMA and commit. K, V and Q arrive by TMA (the
+      // barrier's completion orders them before the MMAs); P is written by
+      // other threads' tcgen05.st, so its wait is followed by the tcgen05
+      // fence that pairs with theirs.
+      // Steps are counted from the CTA's first KV tile (j_start); query tile t
+      // has steps 0 .. n_tiles[t] - j_start - 1 (none if that is not positive).
+      bool good = wait_(bar(kBarQ), 0, abort);
+      int v_ready = -1;  // last step whose V is resident (and tail-zeroed)
+      // This thread shares its SM sub-partition with two softmax warps, which
+      // take most issue slots while they run: every instruction here delays
+      // the next MMA. So the operand descriptors are built once, as 32-bit
+      // low halves over one common high half (all have a 1024-byte stride
+      // between 8-row groups and 128-byte swizzle), and each MMA adds a
+      // constant to the start-address field (address / 16 in the low 14 bits;
+      // no shared-memory address carries out of it).
+      const uint32_t desc_hi = static_cast<uint32_t>(smem_desc_sw128(sQ, 16, 1024) >> 32);
+      auto lo = [](uint64_t d) { return static_cast<uint32_t>(d); };
+      const uint32_t q_lo0 = lo(smem_desc_sw128(sQ, 16, 1024));
+      const uint32_t q_lo1 = lo(smem_desc_sw128(sQ + kTileBytes, 16, 1024));
+      const uint32_t k_lo0 = lo(smem_desc_sw128(sK, 16, 1024));
+      const uint32_t k_lo1 = lo(smem_desc_sw128(sK + kTileBytes, 16, 1024));
+      const uint32_t v_lo0 = lo(smem_desc_sw128(sV, kHalfBytes, 1024));
+      const uint32_t v_lo1 = lo(smem_desc_sw128(sV + kTileBytes, kHalfBytes, 1024));
+      auto issue_s = [&](int t, int jj) -> bool {
+        const int st = jj & 1;
+        if (!wait_(bar(kBarKFull + st), (jj >> 1) & 1, abort)) return false;
+        const uint32_t tS = tmem + t * kBN;
+        const uint32_t qd = t ? q_lo1 : q_lo0;
+        const uint32_t kd = st ? k_lo1 : k_lo0;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off16 = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(tS, qd + off16, kd + off16, desc_hi, kIdescQK, kk > 0);
+        }
+        mma_commit(bar(kBarS + t));
+        return true;
+      };
+      auto issue_pv = [&](int t, int jj) -> bool {
+        const int st = jj & 1;
+        if (v_ready != jj) {
+          // the producer zeroes the tail of the segment's last KV tile
+          const bool tail = Lk - (j_start + jj) * kBN < kBN;
+          if (!(tail ? wait_(bar(kBarVTail), 0, abort)
+                     : wait_(bar(kBarVFull + st), (jj >> 1) & 1, abort)))
+            return false;
+          v_ready = jj;
+        }
+        // P_t of this step is in TMEM once the softmax of tile t has arrived
+        if (!wait_(bar(kBarP + t), jj & 1, abort)) return false;
+        tc_fence_after();
+        const uint32_t tP = tmem + t * kBN;             // P over the first 64 columns of S_t
+        const uint32_t tO = tmem + 2 * kBN + t * kD;
+        const uint32_t vd = st ? v_lo1 : v_lo0;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_bf16_ts(tO, tP + kk * 8, vd + ((kk * 16 * 128) >> 4), desc_hi, kIdescPV,
+                      (jj > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(kBarO + t));
+        return true;
+      };
+      for (int t = 0; good && t < kTiles; ++t)
+        if (n_tiles[t] - j_start > 0) good = issue_s(t, 0);
+      if (good) mma_commit(bar(kBarKEmpty));  // K of step 0 is free once those are done
+      for (int jj = 1; good && jj <= n_steps; ++jj) {
+        // finish step jj-1 for every query tile, starting step jj where needed
+        for (int t = 0; good && t < kTiles; ++t) {
+          if (jj - 1 >= n_tiles[t] - j_start) continue;
+          good = issue_pv(t, jj - 1);
+          if (good && jj < n_tiles[t] - j_start) good = issue_s(t, jj);
+        }
+        // V of step jj-1 has had its last P.V; K of step jj its last S
+        if (good) {
+          mma_commit(bar(kBarVEmpty + ((jj - 1) & 1)));
+          if (jj < n_steps) mma_commit(bar(kBarKEmpty + (jj & 1)));
+        }
+      }
+      if (!good) fail(abort);
+    }
+  } else {
+    setmaxnreg_inc<RegSplit<false>::kSoftmax>();
+    // ------------------------------------------------------------ softmax / epilogue
+    const int t = warp >> 2;                // query tile of this warpgroup
+    const int quad = warp & 3;              // TMEM lane quadrant this warp may access
+    const int r = quad * 32 + lane;         // row within the tile == TMEM lane
+    const int n_t = n_tiles[t] > 0 ? n_tiles[t] - j_start : 0;  // steps of this tile
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + t * kBN + lane_off;
+    const uint32_t tO = tmem + 2 * kBN + t * kD + lane_off;
+    const int qi = row0[t] + r;             // query index within the segment
+    const int lim = diag + qi;              // last key this row may see
+
+    // Running maximum m (log2 units) and two running sums: l of the fp32
+    // probabilities, for the lse, and lr of the same probabilities rounded to
+    // bf16 as the P.V product sees them, which normalises the output. The
+    // maximum is lazy: a row keeps its m while a tile's probabilities sum to
+    // at most 2^kLazyMax, so no probability exceeds that bound and O is
+    // rescaled only when some row of the warp passes it. Dividing by
+    // the sum of the rounded probabilities keeps the output a convex
+    // combination of the V rows with the weights the tensor core used, so a
+    // large probability rounded to bf16 costs no more than it does under an
+    // exact maximum.
+    float m = 0.f, l = 0.f, lr = 0.f;
+    bool good = true;
+    const uint64_t scl = f32x2(p.scale_log2, p.scale_log2);
+    for (int jj = 0; jj < n_t; ++jj) {
+      if (!__all_sync(0xffffffffu, wait_(bar(kBarS + t), jj & 1, abort))) {
+        good = false;
+        break;
+      }
+      tc_fence_after();
+      const int kbase = (j_start + jj) * kBN;
+      uint32_t x[kBN];
+#pragma unroll
+      for (int c = 0; c < kBN; c += 32)
+        tmem_ld32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(&x[c]));
+      tmem_wait_ld();
+      // keys past the row's causal limit or the segment end are masked (their
+      // logit becomes -inf, their probability 0); only the diagonal and the
+      // tail tiles have any
+      if ((kbase + kBN - 1 > diag + row0[t]) || (kbase + kBN > Lk)) {
+        const int keep = min(lim, Lk - 1) - kbase + 1;  // columns < keep are at or before the limit
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if (c >= keep) x[c] = 0xFF800000u;
+      }
+      // P = 2^(x * scale - mm), packed two per column over the first 64
+      // columns of S_t (all of S is already in registers); ts and tr get the
+      // tile's sums of the fp32 and of the bf16-rounded probabilities
+      auto exps = [&](float mm, float &ts, float &tr) {
+        const uint64_t nm = f32x2(-mm, -mm);
+        uint64_t s0 = 0, s1 = 0;
+        float r0l = 0.f, r0h = 0.f, r1l = 0.f, r1h = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int k = hf * 64 + 2 * c;
+            const uint64_t e =
+                fma2(f32x2(__uint_as_float(x[k]), __uint_as_float(x[k + 1])), scl, nm);
+            const float p0 = fast_exp2(f32x2_lo(e)), p1 = fast_exp2(f32x2_hi(e));
+            pk[c] = pack_bf16x2(p0, p1);
+            if (c & 1) {
+              add2(s1, f32x2(p0, p1));
+              add_bf16x2_to_f32(r1l, r1h, pk[c]);
+            } else {
+              add2(s0, f32x2(p0, p1));
+              add_bf16x2_to_f32(r0l, r0h, pk[c]);
+            }
+          }
+          tmem_st32(tS + hf * 32, pk);
+        }
+        add2(s0, s1);
+        ts = f32x2_lo(s0) + f32x2_hi(s0);
+        tr = (r0l + r1l) + (r0h + r1h);
+      };
+      // First with the row's current maximum, without looking for a larger
+      // one: if no row of the warp then has a tile sum above 2^kLazyMax, no
+      // probability exceeds that bound either and the tile is done. Otherwise
+      // (some logit lies more than a little above m; an infinite sum included)
+      // the warp takes the exact maximum, rescales O and recomputes P over
+      // what it wrote. The first tile of a row always takes the maximum.
+      float ts, tr;
+      bool exact = jj == 0;
+#pragma unroll 1
+      for (;;) {
+        if (exact) {
+          // row max of the raw logits (the scale is positive): eight chains
+          // of three-input maxima
+          float a[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a[i] = __uint_as_float(x[i]);
+#pragma unroll
+          for (int c = 8; c < kBN; c += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              a[i] = fmax3(a[i], __uint_as_float(x[c + i]), __uint_as_float(x[c + 8 + i]));
+          const float mx =
+              fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+          const float mxs = mx * p.scale_log2;  // -inf stays -inf
+          if (jj == 0) {
+            // nothing is in O yet; every row sees key 0
+            m = mxs;
+          } else {
+            // P.V of the previous step is complete (this S was issued after
+            // it): rescale the O rows in TMEM. The accesses are warp-wide, so
+            // the whole warp takes its new maxima.
+            const float m_new = fmaxf(m, mxs);
+            const float alpha = fast_exp2(m - m_new);
+            // 32 columns at a time: all of S is held in registers meanwhile
+#pragma unroll 1
+            for (int c = 0; c < kD; c += 32) {
+              uint32_t o[32];
+              tmem_ld32(tO + c, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tO + c, o);
+            }
+            tmem_wait_st();
+            l *= alpha;
+            lr *= alpha;
+            m = m_new;
+          }
+        }
+        exps(m, ts, tr);
+        if (exact || !__any_sync(0xffffffffu, !(ts <= kLazyBound))) break;
+        exact = true;
+      }
+      l += ts;
+      lr += tr;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(kBarP + t));
+    }
+    if (n_t > 0 &&
+        __all_sync(0xffffffffu, good && wait_(bar(kBarO + t), (n_t - 1) & 1, abort))) {
+      tc_fence_after();
+      const float inv_l = 1.f / lr;
+      const bool store = qi < Lq;
+      __nv_bfloat16 *orow =
+          p.out + (static_cast<int64_t>(q0 + qi) * p.num_q_heads + head[t]) * kD;
+#pragma unroll
+      for (int c = 0; c < kD / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_wait_ld();
+        if (store) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[i + 0]) * inv_l, __uint_as_float(o[i + 1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(o[i + 4]) * inv_l, __uint_as_float(o[i + 5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(o[i + 6]) * inv_l, __uint_as_float(o[i + 7]) * inv_l);
+            *reinterpret_cast<uint4 *>(orow + c * 32 + i) = v;
+          }
+        }
+      }
+      if (store && p.lse != nullptr)
+        p.lse[static_cast<int64_t>(q0 + qi) * p.num_q_heads + head[t]] = (m + log2f(l)) * kLn2;
+    } else if (n_t > 0 && r == 0) {
+      fail(abort);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kProducerWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+
+// Persistent: one CTA per SM walks its items. Used with a sliding window,
+// where an item is two or three KV steps and a CTA's fixed cost (a few
+// microseconds of set-up, pipeline fill and drain) would otherwise rival its
+// work. Barrier phases run on across items: K/V stages and the V-tail barriers count the CTA's KV steps, the S,
 // P and O barriers of tile t count that tile's steps, the Q barriers count
 // items. The next item's Q is loaded once every S MMA of the current item has
 // completed (kBarQEmpty), its first S MMAs follow the current item's last
 // P.V in issue order, and its first P.V (which overwrites O) waits for the
 // softmax warps' P, which they write only after reading the current O.
-template <bool kWindowed, bool kPersistent>
+template <bool kWindowed>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap q_map,
+    prefill_persistent_kernel(const __grid_constant__ CUtensorMap q_map,
                    const __grid_constant__ CUtensorMap k_map,
                    const __grid_constant__ CUtensorMap v_map, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -272,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp >= kProducerWarp) {
-    setmaxnreg_dec<RegSplit<kPersistent>::kOther>();
+    setmaxnreg_dec<RegSplit<true>::kOther>();
     if (warp == kProducerWarp && !skipped) {
       // ------------------------------------------------------------ TMA producer
       // Per item: both Q tiles (once the previous item's S MMAs are done with
@@ -289,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&k_map);
         prefetch_tensormap(&v_map);
       }
-      ItemWalk<kWindowed, kPersistent> w;
+      ItemWalk<kWindowed> w;
       int G0 = 0;  // KV steps of earlier items
       bool good = true;
       Item it;
@@ -300,13 +764,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (lane == 0) {
-          if constexpr (kPersistent) {
-            volatile int *dv = reinterpret_cast<volatile int *>(smem + kItemOff);
-            dv[0] = it.n_tiles[0] > 0 ? it.n_tiles[0] - it.j_start : 0;
-            dv[1] = it.n_tiles[1] > 0 ? it.n_tiles[1] - it.j_start : 0;
-            dv[2] = it.n_steps;
-            dv[3] = it.Lk - (it.j_start + it.n_steps - 1) * kBN < kBN ? 1 : 0;
-          }
+          volatile int *dv = reinterpret_cast<volatile int *>(smem + kItemOff);
+          dv[0] = it.n_tiles[0] > 0 ? it.n_tiles[0] - it.j_start : 0;
+          dv[1] = it.n_tiles[1] > 0 ? it.n_tiles[1] - it.j_start : 0;
+          dv[2] = it.n_steps;
+          dv[3] = it.Lk - (it.j_start + it.n_steps - 1) * kBN < kBN ? 1 : 0;
           uint32_t qbytes = 0;
 #pragma unroll
           for (int t = 0; t < kTiles; ++t) qbytes += it.n_tiles[t] > 0 ? kTileBytes : 0;
@@ -394,16 +856,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every copy of this CTA is issued: the next kernel may start launching
       if (lane == 0) griddep_launch_dependents();
-      if constexpr (kPersistent) {
-        // an empty descriptor ends the MMA issuer's walk (once it is done with
-        // the last item's descriptor: its S MMAs have completed)
-        if (good && w.item_no >= 0 &&
-            !__all_sync(0xffffffffu, wait_(bar(kBarQEmpty), w.item_no & 1)))
-          good = false;
-        if (good && lane == 0) {
-          reinterpret_cast<volatile int *>(smem + kItemOff)[2] = 0;  // n_steps
-          mbar_arrive(bar(kBarQ));
-        }
+      // an empty descriptor ends the MMA issuer's walk (once it is done with
+      // the last item's descriptor: its S MMAs have completed)
+      if (good && w.item_no >= 0 &&
+          !__all_sync(0xffffffffu, wait_(bar(kBarQEmpty), w.item_no & 1)))
+        good = false;
+      if (good && lane == 0) {
+        reinterpret_cast<volatile int *>(smem + kItemOff)[2] = 0;  // n_steps
+        mbar_arrive(bar(kBarQ));
       }
       // wait for the last release of each stage, so that no arrival from the
       // tensor core reaches this CTA's shared memory after it has exited
@@ -455,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(bar(kBarS + t));
           // the item's last S: the Q buffer is free for the next item once it completes
-          if (kPersistent && --s_left == 0) mma_commit(bar(kBarQEmpty));
+          if (--s_left == 0) mma_commit(bar(kBarQEmpty));
           return true;
         };
         auto issue_pv = [&](int t, int jj) -> bool {
@@ -509,42 +969,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         return ok;
       };
       bool good = true;
-      if constexpr (kPersistent) {
-        // item by item, as the producer publishes them with their Q
-        int G0 = 0, T00 = 0, T01 = 0;
-        for (int item_no = 0; good; ++item_no) {
-          if (!wait_(bar(kBarQ), item_no & 1)) {
-            good = false;
-            break;
-          }
-          const volatile int *dv = reinterpret_cast<volatile int *>(smem + kItemOff);
-          const int n_t0 = dv[0], n_t1 = dv[1], n_steps = dv[2], tail = dv[3];
-          if (n_steps == 0) break;  // no more items
-          good = run_item(n_t0, n_t1, n_steps, tail != 0, G0, T00, T01);
-          G0 += n_steps;
-          T00 += n_t0;
-          T01 += n_t1;
+      // item by item, as the producer publishes them with their Q
+      int G0 = 0, T00 = 0, T01 = 0;
+      for (int item_no = 0; good; ++item_no) {
+        if (!wait_(bar(kBarQ), item_no & 1)) {
+          good = false;
+          break;
         }
-      } else {
-        Item it;
-        if (make_item<kWindowed>(p, static_cast<int>(blockIdx.x), false, it)) {
-          const int n_t0 = it.n_tiles[0] > 0 ? it.n_tiles[0] - it.j_start : 0;
-          const int n_t1 = it.n_tiles[1] > 0 ? it.n_tiles[1] - it.j_start : 0;
-          const bool tail = it.Lk - (it.j_start + it.n_steps - 1) * kBN < kBN;
-          good = wait_(bar(kBarQ), 0) && run_item(n_t0, n_t1, it.n_steps, tail, 0, 0, 0);
-        }
+        const volatile int *dv = reinterpret_cast<volatile int *>(smem + kItemOff);
+        const int n_t0 = dv[0], n_t1 = dv[1], n_steps = dv[2], tail = dv[3];
+        if (n_steps == 0) break;  // no more items
+        good = run_item(n_t0, n_t1, n_steps, tail != 0, G0, T00, T01);
+        G0 += n_steps;
+        T00 += n_t0;
+        T01 += n_t1;
       }
       // every MMA issued here has completed before the CTA frees its TMEM
-      // (one CTA per item: the softmax warps' waits for the last P.V of each
-      // tile, which follows every other MMA, already ensure it)
-      if (kPersistent) {
-        mma_commit(bar(kBarDone));
-        if (!wait_(bar(kBarDone), 0)) good = false;
-      }
+      mma_commit(bar(kBarDone));
+      if (!wait_(bar(kBarDone), 0)) good = false;
       if (!good) fail();
     }
   } else {
-    setmaxnreg_inc<RegSplit<kPersistent>::kSoftmax>();
+    setmaxnreg_inc<RegSplit<true>::kSoftmax>();
     if (!skipped) {
       // ------------------------------------------------------------ softmax / epilogue
       const int t = warp >> 2;                // query tile of this warpgroup
@@ -737,18 +1183,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       bool good = true;
-      if constexpr (kPersistent) {
-        ItemWalk<kWindowed, kPersistent> w;
-        int T0 = 0;  // steps of this tile in earlier items
-        Item it;
-        while (good && w.next(p, false, it)) {
-          good = run_item(it, T0);
-          const int tiles_t = t ? it.n_tiles[1] : it.n_tiles[0];
-          T0 += tiles_t > 0 ? tiles_t - it.j_start : 0;
-        }
-      } else {
-        Item it;
-        if (make_item<kWindowed>(p, static_cast<int>(blockIdx.x), false, it)) good = run_item(it, 0);
+      ItemWalk<kWindowed> w;
+      int T0 = 0;  // steps of this tile in earlier items
+      Item it;
+      while (good && w.next(p, false, it)) {
+        good = run_item(it, T0);
+        const int tiles_t = t ? it.n_tiles[1] : it.n_tiles[0];
+        T0 += tiles_t > 0 ? tiles_t - it.j_start : 0;
       }
       if (!good && r == 0) fail();
     }
@@ -764,11 +1205,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+// The kernel to launch: prefill_persistent_kernel or prefill_kernel.
+template <bool kWindowed, bool kPersistent>
+constexpr auto prefill_entry() {
+  if constexpr (kPersistent)
+    return prefill_persistent_kernel<kWindowed>;
+  else
+    return prefill_kernel;
+}
+
 template <bool kWindowed, bool kPersistent>
 cudaError_t launch_instance(dim3 grid, const CUtensorMap &q_map, const CUtensorMap &k_map,
                             const CUtensorMap &v_map, const PrefillParams &p,
                             cudaStream_t stream) {
-  auto kern = prefill_kernel<kWindowed, kPersistent>;
+  auto kern = prefill_entry<kWindowed, kPersistent>();
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -776,7 +1226,7 @@ cudaError_t launch_instance(dim3 grid, const CUtensorMap &q_map, const CUtensorM
   // free: launch only a build whose per-thread allocation covers the split
   static const int launch_regs = [] {
     cudaFuncAttributes fa{};
-    return cudaFuncGetAttributes(&fa, prefill_kernel<kWindowed, kPersistent>) == cudaSuccess
+    return cudaFuncGetAttributes(&fa, prefill_entry<kWindowed, kPersistent>()) == cudaSuccess
                ? fa.numRegs
                : 0;
   }();
@@ -820,8 +1270,10 @@ cudaError_t launch_prefill(const PrefillArgs &a, const CUtensorMap &q_map,
     const dim3 grid(static_cast<unsigned>(n_items < a.num_sms ? n_items : a.num_sms));
     return launch_instance<true, true>(grid, q_map, k_map, v_map, p, stream);
   }
-  return launch_instance<false, false>(dim3(static_cast<unsigned>(n_items)), q_map, k_map, v_map,
-                                       p, stream);
+  const dim3 grid = p.n_pairs <= 65535 && p.num_seqs <= 65535
+                       ? dim3(p.n_rowtiles, p.n_pairs, p.num_seqs)
+                       : dim3(static_cast<unsigned>(n_items));
+  return launch_instance<false, false>(grid, q_map, k_map, v_map, p, stream);
 }
 
 cudaError_t prefill_error_word(uint32_t **word) {
