@@ -318,9 +318,12 @@ __global__ void __launch_bounds__((kMaxHG + 2) * 32, 8 / kMaxHG)
         }
       }
     };
-    // with stable inputs the K/V copies of the first stages go out before the
-    // wait for the previous kernel, their q and new rows after it
-    const int pre = p.stable_inputs ? min(NS, n_mine) : 0;
+    // with stable inputs the K/V copies of the first stage go out before the
+    // wait for the previous kernel, its q and new rows after it (one stage:
+    // when every CTA sends out several stages at once, each CTA's first lands
+    // later, behind the others' second and third; measured faster than two or
+    // three)
+    const int pre = p.stable_inputs ? min(1, n_mine) : 0;
     if (p.stable_inputs) {
       Cursor c = cur;
       for (int i = 0; i < pre; ++i) {
