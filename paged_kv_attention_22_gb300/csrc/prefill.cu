@@ -414,23 +414,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            wait_(bar(kBarVEmpty + (jj & 1)), par, abort));
       }
       if (!good && lane == 0) fail(abort);
-    } else if (warp == kMmaWarp && lane == 0) {
+    } else if (warp == kMmaWarp) {
       // ------------------------------------------------------------ MMA issuer
-      // One thread issues every MMA and commit. K, V and Q arrive by TMA (the
-      // barrier's completion orders them before the MMAs); P is written by
-      // other threads' tcgen05.st, so its wait is followed by the tcgen05
-      // fence that pairs with theirs.
+      // The whole warp runs the loop and its waits, so that its control flow
+      // stays warp-uniform; one elected lane (lane 0, always the same one, as
+      // a commit covers the MMAs its own thread issued) issues every MMA and
+      // commit. A lone thread in its own branch measured about 200 cycles
+      // slower per group of eight MMAs, and slower still beside busy softmax
+      // warps, which share this warp's SM sub-partition.
+      // K, V and Q arrive by TMA (the barrier's completion orders them before
+      // the MMAs); P is written by other threads' tcgen05.st, so its wait is
+      // followed by the tcgen05 fence that pairs with theirs.
       // Steps are counted from the CTA's first KV tile (j_start); query tile t
       // has steps 0 .. n_tiles[t] - j_start - 1 (none if that is not positive).
-      bool good = wait_(bar(kBarQ), 0, abort);
+      auto wait_all = [&](uint32_t b, uint32_t parity) {
+        return __all_sync(0xffffffffu, wait_(b, parity, abort));
+      };
+      bool good = wait_all(bar(kBarQ), 0);
       int v_ready = -1;  // last step whose V is resident (and tail-zeroed)
-      // This thread shares its SM sub-partition with two softmax warps, which
-      // take most issue slots while they run: every instruction here delays
-      // the next MMA. So the operand descriptors are built once, as 32-bit
-      // low halves over one common high half (all have a 1024-byte stride
-      // between 8-row groups and 128-byte swizzle), and each MMA adds a
-      // constant to the start-address field (address / 16 in the low 14 bits;
-      // no shared-memory address carries out of it).
+      // The operand descriptors are built once, as 32-bit low halves over one
+      // common high half (all have a 1024-byte stride between 8-row groups
+      // and 128-byte swizzle), and each MMA adds a constant to the
+      // start-address field (address / 16 in the low 14 bits; no
+      // shared-memory address carries out of it).
       const uint32_t desc_hi = static_cast<uint32_t>(smem_desc_sw128(sQ, 16, 1024) >> 32);
       auto lo = [](uint64_t d) { return static_cast<uint32_t>(d); };
       const uint32_t q_lo0 = lo(smem_desc_sw128(sQ, 16, 1024));
@@ -441,16 +447,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t v_lo1 = lo(smem_desc_sw128(sV + kTileBytes, kHalfBytes, 1024));
       auto issue_s = [&](int t, int jj) -> bool {
         const int st = jj & 1;
-        if (!wait_(bar(kBarKFull + st), (jj >> 1) & 1, abort)) return false;
+        if (!wait_all(bar(kBarKFull + st), (jj >> 1) & 1)) return false;
         const uint32_t tS = tmem + t * kBN;
         const uint32_t qd = t ? q_lo1 : q_lo0;
         const uint32_t kd = st ? k_lo1 : k_lo0;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off16 = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-          mma_bf16_ss(tS, qd + off16, kd + off16, desc_hi, kIdescQK, kk > 0);
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off16 = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+            mma_bf16_ss(tS, qd + off16, kd + off16, desc_hi, kIdescQK, kk > 0);
+          }
+          mma_commit(bar(kBarS + t));
         }
-        mma_commit(bar(kBarS + t));
+        __syncwarp();
         return true;
       };
       auto issue_pv = [&](int t, int jj) -> bool {
@@ -458,27 +467,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (v_ready != jj) {
           // the producer zeroes the tail of the segment's last KV tile
           const bool tail = Lk - (j_start + jj) * kBN < kBN;
-          if (!(tail ? wait_(bar(kBarVTail), 0, abort)
-                     : wait_(bar(kBarVFull + st), (jj >> 1) & 1, abort)))
+          if (!(tail ? wait_all(bar(kBarVTail), 0) : wait_all(bar(kBarVFull + st), (jj >> 1) & 1)))
             return false;
           v_ready = jj;
         }
         // P_t of this step is in TMEM once the softmax of tile t has arrived
-        if (!wait_(bar(kBarP + t), jj & 1, abort)) return false;
+        if (!wait_all(bar(kBarP + t), jj & 1)) return false;
         tc_fence_after();
         const uint32_t tP = tmem + t * kBN;             // P over the first 64 columns of S_t
         const uint32_t tO = tmem + 2 * kBN + t * kD;
         const uint32_t vd = st ? v_lo1 : v_lo0;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_bf16_ts(tO, tP + kk * 8, vd + ((kk * 16 * 128) >> 4), desc_hi, kIdescPV,
-                      (jj > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(kBarO + t));
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_bf16_ts(tO, tP + kk * 8, vd + ((kk * 16 * 128) >> 4), desc_hi, kIdescPV,
+                        (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(kBarO + t));
+        }
+        __syncwarp();
         return true;
       };
       for (int t = 0; good && t < kTiles; ++t)
         if (n_tiles[t] - j_start > 0) good = issue_s(t, 0);
-      if (good) mma_commit(bar(kBarKEmpty));  // K of step 0 is free once those are done
+      if (good) {
+        if (elect_one()) mma_commit(bar(kBarKEmpty));  // K of step 0 is free once those are done
+        __syncwarp();
+      }
       for (int jj = 1; good && jj <= n_steps; ++jj) {
         // finish step jj-1 for every query tile, starting step jj where needed
         for (int t = 0; good && t < kTiles; ++t) {
@@ -488,11 +502,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // V of step jj-1 has had its last P.V; K of step jj its last S
         if (good) {
-          mma_commit(bar(kBarVEmpty + ((jj - 1) & 1)));
-          if (jj < n_steps) mma_commit(bar(kBarKEmpty + (jj & 1)));
+          if (elect_one()) {
+            mma_commit(bar(kBarVEmpty + ((jj - 1) & 1)));
+            if (jj < n_steps) mma_commit(bar(kBarKEmpty + (jj & 1)));
+          }
+          __syncwarp();
         }
       }
-      if (!good) fail(abort);
+      if (!good && lane == 0) fail(abort);
     }
   } else {
     setmaxnreg_inc<RegSplit<false>::kSoftmax>();

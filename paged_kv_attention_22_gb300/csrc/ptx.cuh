@@ -128,6 +128,17 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// True in one lane of the (converged) warp: the lowest lane of the full mask.
+// A warp that runs an MMA loop together, with this lane issuing each MMA and
+// commit, keeps its control flow warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 // Allocate ncols TMEM columns (power of two >= 32); the whole warp executes
@@ -195,8 +206,7 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
-// Arrive once on the mbarrier when every tcgen05.mma issued so far by this
-// thread has completed.
+// The same MMA with the shared-memory descriptor given as its two 32-bit halves.
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                             uint32_t desc_hi, uint32_t idesc,
                                             uint32_t accumulate) {
@@ -209,6 +219,8 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Arrive once on the mbarrier when every tcgen05.mma issued so far by this
+// thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
