@@ -890,19 +890,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            wait_(bar(kBarVEmpty + (gk & 1)), par));
       }
       if (!good && lane == 0) fail();
-    } else if (warp == kMmaWarp && lane == 0 && !skipped) {
+    } else if (warp == kMmaWarp && !skipped) {
       // ------------------------------------------------------------ MMA issuer
-      // One thread issues every MMA and commit. K, V and Q arrive by TMA (the
-      // barrier's completion orders them before the MMAs); P is written by
-      // other threads' tcgen05.st, so its wait is followed by the tcgen05
-      // fence that pairs with theirs.
-      // This thread shares its SM sub-partition with two softmax warps, which
-      // take most issue slots while they run: every instruction here delays
-      // the next MMA. So the operand descriptors are built once, as 32-bit
-      // low halves over one common high half (all have a 1024-byte stride
-      // between 8-row groups and 128-byte swizzle), and each MMA adds a
-      // constant to the start-address field (address / 16 in the low 14 bits;
-      // no shared-memory address carries out of it).
+      // As in prefill_kernel: the whole warp runs the loop and its waits
+      // (warp-uniform control flow) and one elected lane, always lane 0,
+      // issues every MMA and commit. K, V and Q arrive by TMA (the barrier's
+      // completion orders them before the MMAs); P is written by other
+      // threads' tcgen05.st, so its wait is followed by the tcgen05 fence
+      // that pairs with theirs.
+      // The operand descriptors are built once, as 32-bit low halves over one
+      // common high half (all have a 1024-byte stride between 8-row groups
+      // and 128-byte swizzle), and each MMA adds a constant to the
+      // start-address field (address / 16 in the low 14 bits; no
+      // shared-memory address carries out of it).
+      auto wait_all = [&](uint32_t b, uint32_t parity) {
+        return __all_sync(0xffffffffu, wait_(b, parity));
+      };
       const uint32_t desc_hi = static_cast<uint32_t>(smem_desc_sw128(sQ, 16, 1024) >> 32);
       auto lo = [](uint64_t d) { return static_cast<uint32_t>(d); };
       const uint32_t q_lo0 = lo(smem_desc_sw128(sQ, 16, 1024));
@@ -921,18 +924,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         int v_ready = -1;          // last step whose V is resident (and tail-zeroed)
         auto issue_s = [&](int t, int jj) -> bool {
           const int gk = G0 + jj, st = gk & 1;
-          if (!wait_(bar(kBarKFull + st), (gk >> 1) & 1)) return false;
+          if (!wait_all(bar(kBarKFull + st), (gk >> 1) & 1)) return false;
           const uint32_t tS = tmem + t * kBN;
           const uint32_t qd = t ? q_lo1 : q_lo0;
           const uint32_t kd = st ? k_lo1 : k_lo0;
+          --s_left;
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t off16 = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-            mma_bf16_ss(tS, qd + off16, kd + off16, desc_hi, kIdescQK, kk > 0);
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t off16 = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+              mma_bf16_ss(tS, qd + off16, kd + off16, desc_hi, kIdescQK, kk > 0);
+            }
+            mma_commit(bar(kBarS + t));
+            // the item's last S: the Q buffer is free for the next item once it completes
+            if (s_left == 0) mma_commit(bar(kBarQEmpty));
           }
-          mma_commit(bar(kBarS + t));
-          // the item's last S: the Q buffer is free for the next item once it completes
-          if (--s_left == 0) mma_commit(bar(kBarQEmpty));
+          __syncwarp();
           return true;
         };
         auto issue_pv = [&](int t, int jj) -> bool {
@@ -943,30 +950,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (has_tail && jj == n_steps - 1) {
               const uint32_t par = (tail_parity >> st) & 1u;
               tail_parity ^= 1u << st;
-              ok = wait_(bar(kBarVTail + st), par);
+              ok = wait_all(bar(kBarVTail + st), par);
             } else {
-              ok = wait_(bar(kBarVFull + st), (gk >> 1) & 1);
+              ok = wait_all(bar(kBarVFull + st), (gk >> 1) & 1);
             }
             if (!ok) return false;
             v_ready = jj;
           }
           // P_t of this step is in TMEM once the softmax of tile t has arrived
-          if (!wait_(bar(kBarP + t), ((t ? T01 : T00) + jj) & 1)) return false;
+          if (!wait_all(bar(kBarP + t), ((t ? T01 : T00) + jj) & 1)) return false;
           tc_fence_after();
           const uint32_t tP = tmem + t * kBN;             // P over the first 64 columns of S_t
           const uint32_t tO = tmem + 2 * kBN + t * kD;
           const uint32_t vd = st ? v_lo1 : v_lo0;
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_bf16_ts(tO, tP + kk * 8, vd + ((kk * 16 * 128) >> 4), desc_hi, kIdescPV,
-                        (jj > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(kBarO + t));
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              mma_bf16_ts(tO, tP + kk * 8, vd + ((kk * 16 * 128) >> 4), desc_hi, kIdescPV,
+                          (jj > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bar(kBarO + t));
+          }
+          __syncwarp();
           return true;
         };
         bool ok = true;
         if (ok && n_t0 > 0) ok = issue_s(0, 0);
         if (ok && n_t1 > 0) ok = issue_s(1, 0);
-        if (ok) mma_commit(bar(kBarKEmpty + (G0 & 1)));  // K of step 0 is free once those are done
+        if (ok) {
+          if (elect_one()) mma_commit(bar(kBarKEmpty + (G0 & 1)));  // K of step 0 is free once those are done
+          __syncwarp();
+        }
         for (int jj = 1; ok && jj <= n_steps; ++jj) {
           // finish step jj-1 for every query tile, starting step jj where needed
           if (jj - 1 < n_t0) {
@@ -979,8 +992,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // V of step jj-1 has had its last P.V; K of step jj its last S
           if (ok) {
-            mma_commit(bar(kBarVEmpty + ((G0 + jj - 1) & 1)));
-            if (jj < n_steps) mma_commit(bar(kBarKEmpty + ((G0 + jj) & 1)));
+            if (elect_one()) {
+              mma_commit(bar(kBarVEmpty + ((G0 + jj - 1) & 1)));
+              if (jj < n_steps) mma_commit(bar(kBarKEmpty + ((G0 + jj) & 1)));
+            }
+            __syncwarp();
           }
         }
         return ok;
@@ -989,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // item by item, as the producer publishes them with their Q
       int G0 = 0, T00 = 0, T01 = 0;
       for (int item_no = 0; good; ++item_no) {
-        if (!wait_(bar(kBarQ), item_no & 1)) {
+        if (!wait_all(bar(kBarQ), item_no & 1)) {
           good = false;
           break;
         }
@@ -1002,9 +1018,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         T01 += n_t1;
       }
       // every MMA issued here has completed before the CTA frees its TMEM
-      mma_commit(bar(kBarDone));
-      if (!wait_(bar(kBarDone), 0)) good = false;
-      if (!good) fail();
+      if (elect_one()) mma_commit(bar(kBarDone));
+      __syncwarp();
+      if (!wait_all(bar(kBarDone), 0)) good = false;
+      if (!good && lane == 0) fail();
     }
   } else {
     setmaxnreg_inc<RegSplit<true>::kSoftmax>();
