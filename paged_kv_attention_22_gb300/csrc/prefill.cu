@@ -318,8 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Lane b < kBN / box_rows owns the b-th box of every KV tile: it reads
       // that box's block-table entry one tile ahead (the read overlaps the
       // wait for a free stage) and issues the box's copies; lane 0 arms the
-      // barriers. K and V stages are released separately: K(j) once every
-      // S = Q K(j)^T is done, V(j) once every P.V(j) is.
+      // barriers. One release per step (from the MMA warp's commit that closes
+      // step r) frees both K(r), after its last S = Q K(r)^T, and V(r - 1),
+      // after its last P.V: K(j) reuses the stage of release j - 2, V(j) that
+      // of release j - 1.
       const int box_rows = p.box_rows;
       const int n_boxes = kBN / box_rows;
       if (lane == 0) {
@@ -369,8 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(kdst, &k_map, bar(kBarKFull + st), 0, g, row);
           tma_load_3d(kdst + kHalfBytes, &k_map, bar(kBarKFull + st), 64, g, row);
         }
+        // V(jj - 2) is released by the commit that closes step jj - 1
         if (jj >= kStages &&
-            !__all_sync(0xffffffffu, wait_(bar(kBarVEmpty + st), ((jj >> 1) - 1) & 1, abort))) {
+            !__all_sync(0xffffffffu,
+                        wait_(bar(kBarKEmpty + ((jj - 1) & 1)), ((jj - 1) >> 1) & 1, abort))) {
           good = false;
           break;
         }
@@ -406,13 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(bar(kBarVTail));
         }
       }
-      // wait for the last release of each stage, so that no arrival from the
+      // wait for the last release of each slot, so that no arrival from the
       // tensor core reaches this CTA's shared memory after it has exited
-      for (int jj = max(n_steps - kStages, 0); good && jj < n_steps; ++jj) {
-        const uint32_t par = (jj >> 1) & 1;
-        good = __all_sync(0xffffffffu, wait_(bar(kBarKEmpty + (jj & 1)), par, abort) &&
-                                           wait_(bar(kBarVEmpty + (jj & 1)), par, abort));
-      }
+      for (int r = max(n_steps - 1, 0); good && r <= n_steps; ++r)
+        good = __all_sync(0xffffffffu, wait_(bar(kBarKEmpty + (r & 1)), (r >> 1) & 1, abort));
       if (!good && lane == 0) fail(abort);
     } else if (warp == kMmaWarp) {
       // ------------------------------------------------------------ MMA issuer
@@ -431,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return __all_sync(0xffffffffu, wait_(b, parity, abort));
       };
       bool good = wait_all(bar(kBarQ), 0);
+      int k_ready = -1;  // last step whose K is resident
       int v_ready = -1;  // last step whose V is resident (and tail-zeroed)
       // The operand descriptors are built once, as 32-bit low halves over one
       // common high half (all have a 1024-byte stride between 8-row groups
@@ -447,7 +449,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t v_lo1 = lo(smem_desc_sw128(sV + kTileBytes, kHalfBytes, 1024));
       auto issue_s = [&](int t, int jj) -> bool {
         const int st = jj & 1;
-        if (!wait_all(bar(kBarKFull + st), (jj >> 1) & 1)) return false;
+        if (k_ready != jj) {
+          if (!wait_all(bar(kBarKFull + st), (jj >> 1) & 1)) return false;
+          k_ready = jj;
+        }
         const uint32_t tS = tmem + t * kBN;
         const uint32_t qd = t ? q_lo1 : q_lo0;
         const uint32_t kd = st ? k_lo1 : k_lo0;
@@ -489,8 +494,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int t = 0; good && t < kTiles; ++t)
         if (n_tiles[t] - j_start > 0) good = issue_s(t, 0);
+      // Release r (slot r & 1 of the kBarKEmpty pair) closes step r: K of
+      // step r has had its last S and V of step r - 1 its last P.V. Release 0
+      // follows the S MMAs of step 0.
       if (good) {
-        if (elect_one()) mma_commit(bar(kBarKEmpty));  // K of step 0 is free once those are done
+        if (elect_one()) mma_commit(bar(kBarKEmpty));
         __syncwarp();
       }
       for (int jj = 1; good && jj <= n_steps; ++jj) {
@@ -500,12 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           good = issue_pv(t, jj - 1);
           if (good && jj < n_tiles[t] - j_start) good = issue_s(t, jj);
         }
-        // V of step jj-1 has had its last P.V; K of step jj its last S
         if (good) {
-          if (elect_one()) {
-            mma_commit(bar(kBarVEmpty + ((jj - 1) & 1)));
-            if (jj < n_steps) mma_commit(bar(kBarKEmpty + (jj & 1)));
-          }
+          if (elect_one()) mma_commit(bar(kBarKEmpty + (jj & 1)));
           __syncwarp();
         }
       }
