@@ -52,9 +52,16 @@ constexpr int kRowBytes = kD * 2;       // 256 bytes of one head's K (or V) row
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kLazyMax = 8.0f;         // log2 units the running max may lag
 constexpr int kMergeFast = 8;            // pieces merged with all loads issued at once
-// warps per merge CTA (2-warp CTAs that fit beside a decode CTA, one per SM,
-// measured slower: each warp then merges more pairs)
-constexpr int kMergeWarps = 4;
+// Warps per merge CTA (one pair each). With many pairs, eight: the merge of a
+// call then occupies fewer SMs, which the next call's decode CTAs find free
+// (4 and 16 warps measured slower on 512 pairs). With fewer than
+// kMergeWideMin pairs, four: there each pair is typically a long context cut
+// into many pieces, and spreading the pairs over more SMs measured faster (64
+// pairs of 19 pieces: 41.8 us a call against 46.0 with eight). 2-warp CTAs
+// small enough to sit beside a decode CTA, one per SM, measured slower.
+constexpr int kMergeWarps = 8;
+constexpr int kMergeWarpsFew = 4;
+constexpr int64_t kMergeWideMin = 256;
 
 struct DecodeParams {
   const uint8_t *q;                // queries [S, H_q, D] (the CTA's first segment reads them directly)
@@ -679,8 +686,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
   // stale: write nothing, as the decode kernel did not
   if (*reinterpret_cast<volatile uint32_t *>(&g_decode_errors) & kErrTimeout) return;
   const int64_t n_pairs = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads;
-  for (int64_t pi = static_cast<int64_t>(blockIdx.x) * kMergeWarps + warp; pi < n_pairs;
-       pi += static_cast<int64_t>(gridDim.x) * kMergeWarps) {
+  const int n_warps = static_cast<int>(blockDim.x >> 5);
+  for (int64_t pi = static_cast<int64_t>(blockIdx.x) * n_warps + warp; pi < n_pairs;
+       pi += static_cast<int64_t>(gridDim.x) * n_warps) {
     const int s = static_cast<int>(pi / p.num_kv_heads), kvh = static_cast<int>(pi % p.num_kv_heads);
     const int hg = kvh / HG, g = kvh % HG;
     const int nch = chunks_of(merge_prefix, s);
@@ -823,8 +831,9 @@ cudaError_t launch_variant(const DecodeArgs &a, const CUtensorMap &k_map,
                  kn_map, vn_map, p);
   if (e != cudaSuccess) return e;
   const int64_t n_pairs = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
-  const int merge_grid = static_cast<int>((n_pairs + kMergeWarps - 1) / kMergeWarps);
-  return launch_pdl(decode_merge_kernel<G>, dim3(merge_grid), dim3(kMergeWarps * 32),
+  const int merge_warps = n_pairs >= kMergeWideMin ? kMergeWarps : kMergeWarpsFew;
+  const int merge_grid = static_cast<int>((n_pairs + merge_warps - 1) / merge_warps);
+  return launch_pdl(decode_merge_kernel<G>, dim3(merge_grid), dim3(merge_warps * 32),
                     sizeof(int) * static_cast<size_t>(a.num_seqs + 1), stream, p, a.grid);
 }
 
