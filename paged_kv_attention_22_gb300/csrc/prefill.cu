@@ -316,12 +316,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
       // ------------------------------------------------------------ TMA producer
       // Lane b < kBN / box_rows owns the b-th box of every KV tile: it reads
-      // that box's block-table entry one tile ahead (the read overlaps the
-      // wait for a free stage) and issues the box's copies; lane 0 arms the
-      // barriers. One release per step (from the MMA warp's commit that closes
-      // step r) frees both K(r), after its last S = Q K(r)^T, and V(r - 1),
-      // after its last P.V: K(j) reuses the stage of release j - 2, V(j) that
-      // of release j - 1.
+      // that box's block-table entry a tile ahead of its copy (the read
+      // overlaps the wait for a free stage) and issues the box's copies; lane 0
+      // arms the barriers. One release per step (the MMA warp's commit that
+      // closes step r) frees both K(r), after its last S = Q K(r)^T, and
+      // V(r - 1), after its last P.V. K(0) goes first, on its own barrier;
+      // then step j's copies, V(j) and K(j + 1), wait for release j - 1 (which
+      // frees both their stages) and share one barrier, so that the MMA warp
+      // waits once per step for its K and V.
       const int box_rows = p.box_rows;
       const int n_boxes = kBN / box_rows;
       if (lane == 0) {
@@ -343,48 +345,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t *table = p.block_tables + static_cast<int64_t>(s) * p.max_blocks;
       auto box_key = [&](int j) { return j * kBN + lane * box_rows; };
       auto has_box = [&](int j) { return lane < n_boxes && j < n_max && box_key(j) < Lk; };
-      int32_t next_blk = has_box(j_start) ? __ldg(table + box_key(j_start) / p.block_size) : -1;
+      auto blk_of = [&](int j) {
+        return has_box(j) ? __ldg(table + box_key(j) / p.block_size) : -1;
+      };
+      // cache row of this lane's box in KV tile j (-1: none; a block outside
+      // the pool is reported and its box left out)
+      auto row_of = [&](int j, int32_t blk) -> int32_t {
+        if (!has_box(j)) return -1;
+        if (blk < 0 || blk >= p.num_blocks) {
+          atomicOr(&g_prefill_errors, kErrBlock);
+          return -1;
+        }
+        return blk * p.block_size + box_key(j) % p.block_size;
+      };
+      auto tile_bytes = [&](int32_t row) {
+        return __popc(__ballot_sync(0xffffffffu, row >= 0)) * 2u * box_rows * 128u;
+      };
+      int32_t row_cur = row_of(j_start, blk_of(j_start));  // KV tile of step jj
+      int32_t blk_nxt = blk_of(j_start + 1);               // and its successor's entry
+      {
+        const uint32_t bytes = tile_bytes(row_cur);
+        if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull), bytes);
+        __syncwarp();
+        if (row_cur >= 0) {
+          const uint32_t kdst = sK + lane * box_rows * 128;
+          tma_load_3d(kdst, &k_map, bar(kBarKFull), 0, g, row_cur);
+          tma_load_3d(kdst + kHalfBytes, &k_map, bar(kBarKFull), 64, g, row_cur);
+        }
+      }
       bool good = true;
       for (int jj = 0; jj < n_steps; ++jj) {
         const int j = j_start + jj;
-        const int st = jj & 1;
-        const int32_t blk = next_blk;
-        if (has_box(j + 1)) next_blk = __ldg(table + box_key(j + 1) / p.block_size);
-        int32_t row = -1;
-        if (has_box(j)) {
-          if (blk < 0 || blk >= p.num_blocks)
-            atomicOr(&g_prefill_errors, kErrBlock);
-          else
-            row = blk * p.block_size + box_key(j) % p.block_size;
-        }
-        const uint32_t bytes =
-            __popc(__ballot_sync(0xffffffffu, row >= 0)) * 2u * box_rows * 128u;
-        if (jj >= kStages &&
-            !__all_sync(0xffffffffu, wait_(bar(kBarKEmpty + st), ((jj >> 1) - 1) & 1, abort))) {
-          good = false;
-          break;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull + st), bytes);
-        __syncwarp();
-        const uint32_t kdst = sK + st * kTileBytes + lane * box_rows * 128;
-        if (row >= 0) {
-          tma_load_3d(kdst, &k_map, bar(kBarKFull + st), 0, g, row);
-          tma_load_3d(kdst + kHalfBytes, &k_map, bar(kBarKFull + st), 64, g, row);
-        }
-        // V(jj - 2) is released by the commit that closes step jj - 1
-        if (jj >= kStages &&
+        const int32_t row_nxt = row_of(j + 1, blk_nxt);  // -1 past the last tile
+        blk_nxt = blk_of(j + 2);
+        const uint32_t bytes = tile_bytes(row_cur) + tile_bytes(row_nxt);
+        if (jj >= 1 &&
             !__all_sync(0xffffffffu,
                         wait_(bar(kBarKEmpty + ((jj - 1) & 1)), ((jj - 1) >> 1) & 1, abort))) {
           good = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(bar(kBarVFull + st), bytes);
+        const uint32_t b = bar(kBarVFull + (jj & 1));
+        if (lane == 0) mbar_arrive_expect_tx(b, bytes);
         __syncwarp();
-        const uint32_t vdst = sV + st * kTileBytes + lane * box_rows * 128;
-        if (row >= 0) {
-          tma_load_3d(vdst, &v_map, bar(kBarVFull + st), 0, g, row);
-          tma_load_3d(vdst + kHalfBytes, &v_map, bar(kBarVFull + st), 64, g, row);
+        if (row_cur >= 0) {
+          const uint32_t vdst = sV + (jj & 1) * kTileBytes + lane * box_rows * 128;
+          tma_load_3d(vdst, &v_map, b, 0, g, row_cur);
+          tma_load_3d(vdst + kHalfBytes, &v_map, b, 64, g, row_cur);
         }
+        if (row_nxt >= 0) {
+          const uint32_t kdst = sK + ((jj + 1) & 1) * kTileBytes + lane * box_rows * 128;
+          tma_load_3d(kdst, &k_map, b, 0, g, row_nxt);
+          tma_load_3d(kdst + kHalfBytes, &k_map, b, 64, g, row_nxt);
+        }
+        row_cur = row_nxt;
       }
       // every copy of this CTA is issued: the next kernel may start launching
       if (lane == 0) griddep_launch_dependents();
@@ -431,31 +445,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait_all = [&](uint32_t b, uint32_t parity) {
         return __all_sync(0xffffffffu, wait_(b, parity, abort));
       };
-      bool good = wait_all(bar(kBarQ), 0);
-      int k_ready = -1;  // last step whose K is resident
-      int v_ready = -1;  // last step whose V is resident (and tail-zeroed)
-      // The operand descriptors are built once, as 32-bit low halves over one
-      // common high half (all have a 1024-byte stride between 8-row groups
-      // and 128-byte swizzle), and each MMA adds a constant to the
-      // start-address field (address / 16 in the low 14 bits; no
-      // shared-memory address carries out of it).
+      // Q and K(0) first; then at the head of step jj one wait covers V(jj - 1)
+      // and K(jj), which the producer copies on one barrier
+      bool good = wait_all(bar(kBarQ), 0) && wait_all(bar(kBarKFull), 0);
+      // The operand descriptors are 32-bit low halves over one common high half
+      // (all have a 1024-byte stride between 8-row groups and 128-byte
+      // swizzle). Every one differs from Q's first by a constant (its offset
+      // / 16 in the start-address field, the low 14 bits, which no
+      // shared-memory address carries out of; for V also the larger leading
+      // byte offset, bits 16-29), so the warp keeps one base and each MMA adds
+      // an immediate.
       const uint32_t desc_hi = static_cast<uint32_t>(smem_desc_sw128(sQ, 16, 1024) >> 32);
-      auto lo = [](uint64_t d) { return static_cast<uint32_t>(d); };
-      const uint32_t q_lo0 = lo(smem_desc_sw128(sQ, 16, 1024));
-      const uint32_t q_lo1 = lo(smem_desc_sw128(sQ + kTileBytes, 16, 1024));
-      const uint32_t k_lo0 = lo(smem_desc_sw128(sK, 16, 1024));
-      const uint32_t k_lo1 = lo(smem_desc_sw128(sK + kTileBytes, 16, 1024));
-      const uint32_t v_lo0 = lo(smem_desc_sw128(sV, kHalfBytes, 1024));
-      const uint32_t v_lo1 = lo(smem_desc_sw128(sV + kTileBytes, kHalfBytes, 1024));
-      auto issue_s = [&](int t, int jj) -> bool {
+      const uint32_t q_lo0 = static_cast<uint32_t>(smem_desc_sw128(sQ, 16, 1024));
+      constexpr uint32_t kVLbo = static_cast<uint32_t>((kHalfBytes - 16) >> 4) << 16;
+      auto desc = [&](int off) { return q_lo0 + static_cast<uint32_t>(off >> 4); };
+      auto issue_s = [&](int t, int jj) {
         const int st = jj & 1;
-        if (k_ready != jj) {
-          if (!wait_all(bar(kBarKFull + st), (jj >> 1) & 1)) return false;
-          k_ready = jj;
-        }
         const uint32_t tS = tmem + t * kBN;
-        const uint32_t qd = t ? q_lo1 : q_lo0;
-        const uint32_t kd = st ? k_lo1 : k_lo0;
+        const uint32_t qd = desc(kQOff + t * kTileBytes);
+        const uint32_t kd = desc(kKOff + st * kTileBytes);
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
@@ -465,23 +473,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(bar(kBarS + t));
         }
         __syncwarp();
-        return true;
       };
       auto issue_pv = [&](int t, int jj) -> bool {
         const int st = jj & 1;
-        if (v_ready != jj) {
-          // the producer zeroes the tail of the segment's last KV tile
-          const bool tail = Lk - (j_start + jj) * kBN < kBN;
-          if (!(tail ? wait_all(bar(kBarVTail), 0) : wait_all(bar(kBarVFull + st), (jj >> 1) & 1)))
-            return false;
-          v_ready = jj;
-        }
         // P_t of this step is in TMEM once the softmax of tile t has arrived
         if (!wait_all(bar(kBarP + t), jj & 1)) return false;
         tc_fence_after();
         const uint32_t tP = tmem + t * kBN;             // P over the first 64 columns of S_t
         const uint32_t tO = tmem + 2 * kBN + t * kD;
-        const uint32_t vd = st ? v_lo1 : v_lo0;
+        const uint32_t vd = desc(kVOff + st * kTileBytes) + kVLbo;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       for (int t = 0; good && t < kTiles; ++t)
-        if (n_tiles[t] - j_start > 0) good = issue_s(t, 0);
+        if (n_tiles[t] - j_start > 0) issue_s(t, 0);
       // Release r (slot r & 1 of the kBarKEmpty pair) closes step r: K of
       // step r has had its last S and V of step r - 1 its last P.V. Release 0
       // follows the S MMAs of step 0.
@@ -502,11 +502,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       for (int jj = 1; good && jj <= n_steps; ++jj) {
+        // V(jj - 1) and K(jj) are resident; the producer zeroes the tail of
+        // the segment's last KV tile, which comes with no K
+        const int b = jj - 1;
+        const bool tail = Lk - (j_start + b) * kBN < kBN;
+        good = tail ? wait_all(bar(kBarVTail), 0)
+                    : wait_all(bar(kBarVFull + (b & 1)), (b >> 1) & 1);
         // finish step jj-1 for every query tile, starting step jj where needed
         for (int t = 0; good && t < kTiles; ++t) {
-          if (jj - 1 >= n_tiles[t] - j_start) continue;
-          good = issue_pv(t, jj - 1);
-          if (good && jj < n_tiles[t] - j_start) good = issue_s(t, jj);
+          if (b >= n_tiles[t] - j_start) continue;
+          good = issue_pv(t, b);
+          if (good && jj < n_tiles[t] - j_start) issue_s(t, jj);
         }
         if (good) {
           if (elect_one()) mma_commit(bar(kBarKEmpty + (jj & 1)));
