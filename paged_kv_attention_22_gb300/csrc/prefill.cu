@@ -74,7 +74,11 @@ constexpr int kAbortOff = kTmemSlotOff + 8;
 // tiles 0 and 1, KV steps (0: no more items), 1 if the last KV tile extends
 // past the segment's last key
 constexpr int kItemOff = kAbortOff + 8;
-constexpr int kSmemBytes = kItemOff + 32 + 1024;  // + slack for 1024-byte alignment
+// the output staging areas of the eight softmax warps: 32 rows of 128 bytes
+constexpr int kEpiWarpBytes = 32 * 128;
+constexpr int kEpiOff = (kItemOff + 32 + 127) / 128 * 128;
+constexpr int kSmemBytes = kEpiOff + 8 * kEpiWarpBytes + 1024;  // + slack for 1024-byte alignment
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 // warps 0-7 softmax (warpgroup t for query tile t), warp 8 TMA producer,
 // warp 9 MMA issuer, warps 10-11 idle: three warpgroups, so that setmaxnreg
 // can move registers from the third to the two softmax warpgroups
@@ -117,6 +121,57 @@ __device__ __forceinline__ bool wait_(uint32_t bar, uint32_t parity, const volat
 __device__ __forceinline__ void fail(volatile int *abort) {
   *abort = 1;
   atomicOr(&g_prefill_errors, kErrTimeout);
+}
+
+// The warp's 32 normalised O rows (its TMEM lane quadrant, 128 fp32 columns)
+// as bf16 rows in global memory: row i of the warp goes to out_w + i *
+// row_stride, for i < n_valid. Each thread holds one row and rows lie
+// row_stride elements apart, so a store straight from registers writes 32
+// lines per instruction. The rows go through the warp's staging area (scr,
+// 32 rows of 128 bytes, one column half at a time) instead: written one row
+// per thread, read back so that each store writes four whole 128-byte row
+// halves. A 16-byte chunk c of row i sits at position c ^ (i & 7), which
+// keeps both sides free of shared-memory bank conflicts.
+__device__ __forceinline__ void store_o_rows(uint32_t tO, float inv_l, uint32_t scr,
+                                             __nv_bfloat16 *out_w, int64_t row_stride,
+                                             int n_valid, int lane) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t o[32];
+      tmem_ld32(tO + h * 64 + q * 32, o);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t w0 = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l,
+                                        __uint_as_float(o[8 * k + 1]) * inv_l);
+        const uint32_t w1 = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l,
+                                        __uint_as_float(o[8 * k + 3]) * inv_l);
+        const uint32_t w2 = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l,
+                                        __uint_as_float(o[8 * k + 5]) * inv_l);
+        const uint32_t w3 = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l,
+                                        __uint_as_float(o[8 * k + 7]) * inv_l);
+        const uint32_t addr = scr + lane * 128 + (((q * 4 + k) ^ (lane & 7)) * 16);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1),
+                     "r"(w2), "r"(w3)
+                     : "memory");
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int row = 4 * i + (lane >> 3), c = lane & 7;
+      uint4 v;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "r"(scr + row * 128 + ((c ^ (row & 7)) * 16))
+                   : "memory");
+      if (row < n_valid)
+        *reinterpret_cast<uint4 *>(out_w + row * row_stride + h * 64 + c * 8) = v;
+    }
+    __syncwarp();
+  }
 }
 
 // One work item: two 128-row query tiles that share every K/V tile. With
@@ -663,25 +718,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = 1.f / lr;
       const bool store = qi < Lq;
-      __nv_bfloat16 *orow =
-          p.out + (static_cast<int64_t>(q0 + qi) * p.num_q_heads + head[t]) * kD;
-#pragma unroll
-      for (int c = 0; c < kD / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + c * 32, o);
-        tmem_wait_ld();
-        if (store) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[i + 0]) * inv_l, __uint_as_float(o[i + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(o[i + 4]) * inv_l, __uint_as_float(o[i + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(o[i + 6]) * inv_l, __uint_as_float(o[i + 7]) * inv_l);
-            *reinterpret_cast<uint4 *>(orow + c * 32 + i) = v;
-          }
-        }
-      }
+      const int qw = row0[t] + quad * 32;  // query of the warp's first row
+      store_o_rows(tO, inv_l, sbase + kEpiOff + warp * kEpiWarpBytes,
+                   p.out + (static_cast<int64_t>(q0 + qw) * p.num_q_heads + head[t]) * kD,
+                   static_cast<int64_t>(p.num_q_heads) * kD, min(32, Lq - qw), lane);
       if (store && p.lse != nullptr)
         p.lse[static_cast<int64_t>(q0 + qi) * p.num_q_heads + head[t]] = (m + log2f(l)) * kLn2;
     } else if (n_t > 0 && r == 0) {
@@ -1201,25 +1241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const float inv_l = 1.f / lr;
           const bool store = qi < Lq;
-          __nv_bfloat16 *orow =
-              p.out + (static_cast<int64_t>(q0 + qi) * p.num_q_heads + head_t) * kD;
-#pragma unroll
-          for (int c = 0; c < kD / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_wait_ld();
-            if (store) {
-#pragma unroll
-              for (int i = 0; i < 32; i += 8) {
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(o[i + 0]) * inv_l, __uint_as_float(o[i + 1]) * inv_l);
-                v.y = pack_bf16x2(__uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
-                v.z = pack_bf16x2(__uint_as_float(o[i + 4]) * inv_l, __uint_as_float(o[i + 5]) * inv_l);
-                v.w = pack_bf16x2(__uint_as_float(o[i + 6]) * inv_l, __uint_as_float(o[i + 7]) * inv_l);
-                *reinterpret_cast<uint4 *>(orow + c * 32 + i) = v;
-              }
-            }
-          }
+          const int qw = row0 + quad * 32;  // query of the warp's first row
+          store_o_rows(tO, inv_l, sbase + kEpiOff + warp * kEpiWarpBytes,
+                       p.out + (static_cast<int64_t>(q0 + qw) * p.num_q_heads + head_t) * kD,
+                       static_cast<int64_t>(p.num_q_heads) * kD, min(32, Lq - qw), lane);
           if (store && p.lse != nullptr)
             p.lse[static_cast<int64_t>(q0 + qi) * p.num_q_heads + head_t] =
                 (m + log2f(l)) * kLn2;
