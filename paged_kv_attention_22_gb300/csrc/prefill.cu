@@ -85,13 +85,13 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 // registers per thread after the split, 2 * softmax + other = 3 * 168 (the
-// launch's share per thread of the 64K register file for 384 threads): the
-// persistent kernel's producer and MMA loops also keep their walk over the
-// items in registers, which 88 holds without spills
+// launch's share per thread of the 64K register file for 384 threads); the
+// same in both kernels (the persistent one's producer and MMA warp, which
+// reads each item from shared memory, fit in 72 without spills)
 template <bool kPersistent>
 struct RegSplit {
-  static constexpr int kSoftmax = kPersistent ? 208 : 216;
-  static constexpr int kOther = kPersistent ? 88 : 72;
+  static constexpr int kSoftmax = 216;
+  static constexpr int kOther = 72;
   static_assert(2 * kSoftmax + kOther == 3 * 168, "register split");
 };
 constexpr uint32_t kTmemCols = 512;            // S0, S1, O0, O1: 128 columns each
@@ -1086,6 +1086,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t scl = f32x2(p.scale_log2, p.scale_log2);
       // One item's softmax and epilogue for this tile; T0 counts the tile's
       // steps before it (0 without persistence). False if a wait gave up.
+      // The walk to the next item (a few global loads and divisions) runs in
+      // the middle of this one: after the tile's last P, while its last P.V
+      // completes, instead of between the epilogue and the next item's start.
+      ItemWalk<kWindowed> w;
+      Item nxt;
+      bool have_nxt = false;
       auto run_item = [&](const Item &it, int T0) -> bool {
         bool good = true;
         // this tile's part of the item, in scalars (selects, not indexed arrays)
@@ -1233,6 +1239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar(kBarP + t));
         }
         if (!good) return false;
+        have_nxt = w.next(p, false, nxt);
         if (n_t > 0) {
           // epilogue: the last P.V of the item has completed once its O barrier
           // phase has; the next item's first P.V (which overwrites O) waits for
@@ -1252,13 +1259,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       bool good = true;
-      ItemWalk<kWindowed> w;
       int T0 = 0;  // steps of this tile in earlier items
       Item it;
-      while (good && w.next(p, false, it)) {
+      bool have = w.next(p, false, it);
+      while (good && have) {
         good = run_item(it, T0);
         const int tiles_t = t ? it.n_tiles[1] : it.n_tiles[0];
         T0 += tiles_t > 0 ? tiles_t - it.j_start : 0;
+        it = nxt;
+        have = have_nxt;
       }
       if (!good && r == 0) fail();
     }
