@@ -61,12 +61,15 @@ constexpr int kKOff = kQOff + kTiles * kTileBytes;
 constexpr int kVOff = kKOff + kStages * kTileBytes;
 constexpr int kBarOff = kVOff + kStages * kTileBytes;
 // barrier slots (8 bytes each)
+// kBarK0: K of the first KV step (of the CTA, or of each item of the
+// persistent kernel); kBarKV + (g & 1): V of step g and K of step g + 1, when
+// that step belongs to the same item; kBarRel + (r & 1): release r, the MMA
+// warp's commit after the S MMAs of step r, which frees K(r) and V(r - 1);
 // kBarVTail + st: the item's last V tile in stage st, its rows past the
 // segment's end zeroed; kBarQEmpty: the item's S MMAs are done with Q;
 // kBarDone: every MMA of the CTA has completed
-constexpr int kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKEmpty = 5, kBarVEmpty = 7, kBarS = 9,
-              kBarP = 11, kBarO = 13, kBarVTail = 15, kBarQEmpty = 17, kBarDone = 18,
-              kNumBars = 19;
+constexpr int kBarQ = 0, kBarK0 = 1, kBarKV = 2, kBarRel = 4, kBarS = 6, kBarP = 8, kBarO = 10,
+              kBarVTail = 12, kBarQEmpty = 14, kBarDone = 15, kNumBars = 16;
 constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
 constexpr int kAbortOff = kTmemSlotOff + 8;
 // the persistent kernel's current item as the MMA issuer needs it, published
@@ -343,11 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(bar(kBarQ), 1);
     mbar_init(bar(kBarVTail), 1);
+    mbar_init(bar(kBarK0), 1);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(kBarKFull + i), 1);
-      mbar_init(bar(kBarVFull + i), 1);
-      mbar_init(bar(kBarKEmpty + i), 1);
-      mbar_init(bar(kBarVEmpty + i), 1);
+      mbar_init(bar(kBarKV + i), 1);
+      mbar_init(bar(kBarRel + i), 1);
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(bar(kBarS + t), 1);
@@ -420,12 +422,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t blk_nxt = blk_of(j_start + 1);               // and its successor's entry
       {
         const uint32_t bytes = tile_bytes(row_cur);
-        if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull), bytes);
+        if (lane == 0) mbar_arrive_expect_tx(bar(kBarK0), bytes);
         __syncwarp();
         if (row_cur >= 0) {
           const uint32_t kdst = sK + lane * box_rows * 128;
-          tma_load_3d(kdst, &k_map, bar(kBarKFull), 0, g, row_cur);
-          tma_load_3d(kdst + kHalfBytes, &k_map, bar(kBarKFull), 64, g, row_cur);
+          tma_load_3d(kdst, &k_map, bar(kBarK0), 0, g, row_cur);
+          tma_load_3d(kdst + kHalfBytes, &k_map, bar(kBarK0), 64, g, row_cur);
         }
       }
       bool good = true;
@@ -436,11 +438,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bytes = tile_bytes(row_cur) + tile_bytes(row_nxt);
         if (jj >= 1 &&
             !__all_sync(0xffffffffu,
-                        wait_(bar(kBarKEmpty + ((jj - 1) & 1)), ((jj - 1) >> 1) & 1, abort))) {
+                        wait_(bar(kBarRel + ((jj - 1) & 1)), ((jj - 1) >> 1) & 1, abort))) {
           good = false;
           break;
         }
-        const uint32_t b = bar(kBarVFull + (jj & 1));
+        const uint32_t b = bar(kBarKV + (jj & 1));
         if (lane == 0) mbar_arrive_expect_tx(b, bytes);
         __syncwarp();
         if (row_cur >= 0) {
@@ -463,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tail_r0 = Lk - (n_max - 1) * kBN;
       if (good && tail_r0 < kBN) {
         const int st = (n_steps - 1) & 1;
-        good = __all_sync(0xffffffffu, wait_(bar(kBarVFull + st), ((n_steps - 1) >> 1) & 1, abort));
+        good = __all_sync(0xffffffffu, wait_(bar(kBarKV + st), ((n_steps - 1) >> 1) & 1, abort));
         if (good) {
           const uint32_t vbase = sV + st * kTileBytes;
           const int n16 = (kBN - tail_r0) * 16;  // 16-byte pieces over both column halves
@@ -482,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // wait for the last release of each slot, so that no arrival from the
       // tensor core reaches this CTA's shared memory after it has exited
       for (int r = max(n_steps - 1, 0); good && r <= n_steps; ++r)
-        good = __all_sync(0xffffffffu, wait_(bar(kBarKEmpty + (r & 1)), (r >> 1) & 1, abort));
+        good = __all_sync(0xffffffffu, wait_(bar(kBarRel + (r & 1)), (r >> 1) & 1, abort));
       if (!good && lane == 0) fail(abort);
     } else if (warp == kMmaWarp) {
       // ------------------------------------------------------------ MMA issuer
@@ -502,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // Q and K(0) first; then at the head of step jj one wait covers V(jj - 1)
       // and K(jj), which the producer copies on one barrier
-      bool good = wait_all(bar(kBarQ), 0) && wait_all(bar(kBarKFull), 0);
+      bool good = wait_all(bar(kBarQ), 0) && wait_all(bar(kBarK0), 0);
       // The operand descriptors are 32-bit low halves over one common high half
       // (all have a 1024-byte stride between 8-row groups and 128-byte
       // swizzle). Every one differs from Q's first by a constant (its offset
@@ -549,11 +551,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int t = 0; good && t < kTiles; ++t)
         if (n_tiles[t] - j_start > 0) issue_s(t, 0);
-      // Release r (slot r & 1 of the kBarKEmpty pair) closes step r: K of
+      // Release r (slot r & 1 of the kBarRel pair) closes step r: K of
       // step r has had its last S and V of step r - 1 its last P.V. Release 0
       // follows the S MMAs of step 0.
       if (good) {
-        if (elect_one()) mma_commit(bar(kBarKEmpty));
+        if (elect_one()) mma_commit(bar(kBarRel));
         __syncwarp();
       }
       for (int jj = 1; good && jj <= n_steps; ++jj) {
@@ -562,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = jj - 1;
         const bool tail = Lk - (j_start + b) * kBN < kBN;
         good = tail ? wait_all(bar(kBarVTail), 0)
-                    : wait_all(bar(kBarVFull + (b & 1)), (b >> 1) & 1);
+                    : wait_all(bar(kBarKV + (b & 1)), (b >> 1) & 1);
         // finish step jj-1 for every query tile, starting step jj where needed
         for (int t = 0; good && t < kTiles; ++t) {
           if (b >= n_tiles[t] - j_start) continue;
@@ -570,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (good && jj < n_tiles[t] - j_start) issue_s(t, jj);
         }
         if (good) {
-          if (elect_one()) mma_commit(bar(kBarKEmpty + (jj & 1)));
+          if (elect_one()) mma_commit(bar(kBarRel + (jj & 1)));
           __syncwarp();
         }
       }
@@ -766,11 +768,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(bar(kBarQ), 1);
     mbar_init(bar(kBarQEmpty), 1);
+    mbar_init(bar(kBarK0), 1);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(kBarKFull + i), 1);
-      mbar_init(bar(kBarVFull + i), 1);
-      mbar_init(bar(kBarKEmpty + i), 1);
-      mbar_init(bar(kBarVEmpty + i), 1);
+      mbar_init(bar(kBarKV + i), 1);
+      mbar_init(bar(kBarRel + i), 1);
       mbar_init(bar(kBarVTail + i), 1);
     }
     for (int t = 0; t < kTiles; ++t) {
@@ -850,50 +851,73 @@ __global__ void __launch_bounds__(kThreads, 1)
                         it.q0 + it.row0[t]);
           }
         }
+        // Release r (the MMA warp's commit after the S MMAs of global step r)
+        // frees K(r) and V(r - 1). The item's first K goes on its own barrier
+        // once release G0 - 2 has freed its stage; then step gk's copies,
+        // V(gk) and (within the item) K(gk + 1), wait for release gk - 1,
+        // which frees both their stages, and share one barrier.
         const int n_max = it.j_start + it.n_steps;
         const int32_t *table = p.block_tables + static_cast<int64_t>(it.s) * p.max_blocks;
         auto box_key = [&](int j) { return j * kBN + lane * box_rows; };
         auto has_box = [&](int j) { return lane < n_boxes && j < n_max && box_key(j) < it.Lk; };
-        int32_t next_blk =
-            has_box(it.j_start) ? __ldg(table + box_key(it.j_start) / p.block_size) : -1;
+        auto blk_of = [&](int j) {
+          return has_box(j) ? __ldg(table + box_key(j) / p.block_size) : -1;
+        };
+        // cache row of this lane's box in KV tile j (-1: none; a block outside
+        // the pool is reported and its box left out)
+        auto row_of = [&](int j, int32_t blk) -> int32_t {
+          if (!has_box(j)) return -1;
+          if (blk < 0 || blk >= p.num_blocks) {
+            atomicOr(&g_prefill_errors, kErrBlock);
+            return -1;
+          }
+          return blk * p.block_size + box_key(j) % p.block_size;
+        };
+        auto tile_bytes = [&](int32_t row) {
+          return __popc(__ballot_sync(0xffffffffu, row >= 0)) * 2u * box_rows * 128u;
+        };
+        int32_t row_cur = row_of(it.j_start, blk_of(it.j_start));
+        int32_t blk_nxt = blk_of(it.j_start + 1);
+        if (G0 >= 2 &&
+            !__all_sync(0xffffffffu, wait_(bar(kBarRel + (G0 & 1)), ((G0 - 2) >> 1) & 1))) {
+          good = false;
+          break;
+        }
+        {
+          const uint32_t bytes = tile_bytes(row_cur);
+          if (lane == 0) mbar_arrive_expect_tx(bar(kBarK0), bytes);
+          __syncwarp();
+          if (row_cur >= 0) {
+            const uint32_t kdst = sK + (G0 & 1) * kTileBytes + lane * box_rows * 128;
+            tma_load_3d(kdst, &k_map, bar(kBarK0), 0, it.g, row_cur);
+            tma_load_3d(kdst + kHalfBytes, &k_map, bar(kBarK0), 64, it.g, row_cur);
+          }
+        }
         for (int jj = 0; jj < it.n_steps; ++jj) {
           const int j = it.j_start + jj, gk = G0 + jj;
-          const int st = gk & 1;
-          const int32_t blk = next_blk;
-          if (has_box(j + 1)) next_blk = __ldg(table + box_key(j + 1) / p.block_size);
-          int32_t row = -1;
-          if (has_box(j)) {
-            if (blk < 0 || blk >= p.num_blocks)
-              atomicOr(&g_prefill_errors, kErrBlock);
-            else
-              row = blk * p.block_size + box_key(j) % p.block_size;
-          }
-          const uint32_t bytes =
-              __popc(__ballot_sync(0xffffffffu, row >= 0)) * 2u * box_rows * 128u;
-          if (gk >= kStages &&
-              !__all_sync(0xffffffffu, wait_(bar(kBarKEmpty + st), ((gk >> 1) - 1) & 1))) {
+          const int32_t row_nxt = row_of(j + 1, blk_nxt);  // -1 past the item's last tile
+          blk_nxt = blk_of(j + 2);
+          const uint32_t bytes = tile_bytes(row_cur) + tile_bytes(row_nxt);
+          if (gk >= 1 &&
+              !__all_sync(0xffffffffu,
+                          wait_(bar(kBarRel + ((gk - 1) & 1)), ((gk - 1) >> 1) & 1))) {
             good = false;
             break;
           }
-          if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull + st), bytes);
+          const uint32_t b = bar(kBarKV + (gk & 1));
+          if (lane == 0) mbar_arrive_expect_tx(b, bytes);
           __syncwarp();
-          const uint32_t kdst = sK + st * kTileBytes + lane * box_rows * 128;
-          if (row >= 0) {
-            tma_load_3d(kdst, &k_map, bar(kBarKFull + st), 0, it.g, row);
-            tma_load_3d(kdst + kHalfBytes, &k_map, bar(kBarKFull + st), 64, it.g, row);
+          if (row_cur >= 0) {
+            const uint32_t vdst = sV + (gk & 1) * kTileBytes + lane * box_rows * 128;
+            tma_load_3d(vdst, &v_map, b, 0, it.g, row_cur);
+            tma_load_3d(vdst + kHalfBytes, &v_map, b, 64, it.g, row_cur);
           }
-          if (gk >= kStages &&
-              !__all_sync(0xffffffffu, wait_(bar(kBarVEmpty + st), ((gk >> 1) - 1) & 1))) {
-            good = false;
-            break;
+          if (row_nxt >= 0) {
+            const uint32_t kdst = sK + ((gk + 1) & 1) * kTileBytes + lane * box_rows * 128;
+            tma_load_3d(kdst, &k_map, b, 0, it.g, row_nxt);
+            tma_load_3d(kdst + kHalfBytes, &k_map, b, 64, it.g, row_nxt);
           }
-          if (lane == 0) mbar_arrive_expect_tx(bar(kBarVFull + st), bytes);
-          __syncwarp();
-          const uint32_t vdst = sV + st * kTileBytes + lane * box_rows * 128;
-          if (row >= 0) {
-            tma_load_3d(vdst, &v_map, bar(kBarVFull + st), 0, it.g, row);
-            tma_load_3d(vdst + kHalfBytes, &v_map, bar(kBarVFull + st), 64, it.g, row);
-          }
+          row_cur = row_nxt;
         }
         if (!good) break;
         // V rows of the item's last tile past the segment's last key (poison
@@ -902,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tail_r0 = it.Lk - (n_max - 1) * kBN;
         if (tail_r0 < kBN) {
           const int gk = G0 + it.n_steps - 1, st = gk & 1;
-          if (!__all_sync(0xffffffffu, wait_(bar(kBarVFull + st), (gk >> 1) & 1))) {
+          if (!__all_sync(0xffffffffu, wait_(bar(kBarKV + st), (gk >> 1) & 1))) {
             good = false;
             break;
           }
@@ -932,13 +956,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         reinterpret_cast<volatile int *>(smem + kItemOff)[2] = 0;  // n_steps
         mbar_arrive(bar(kBarQ));
       }
-      // wait for the last release of each stage, so that no arrival from the
-      // tensor core reaches this CTA's shared memory after it has exited
-      for (int gk = max(G0 - kStages, 0); good && gk < G0; ++gk) {
-        const uint32_t par = (gk >> 1) & 1;
-        good = __all_sync(0xffffffffu, wait_(bar(kBarKEmpty + (gk & 1)), par) &&
-                                           wait_(bar(kBarVEmpty + (gk & 1)), par));
-      }
+      // wait for the last release of each slot (the MMA warp's final commit is
+      // release G0), so that no arrival from the tensor core reaches this
+      // CTA's shared memory after it has exited
+      for (int r = max(G0 - 1, 0); good && G0 > 0 && r <= G0; ++r)
+        good = __all_sync(0xffffffffu, wait_(bar(kBarRel + (r & 1)), (r >> 1) & 1));
       if (!good && lane == 0) fail();
     } else if (warp == kMmaWarp && !skipped) {
       // ------------------------------------------------------------ MMA issuer
@@ -969,12 +991,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // KV steps; G0, T00 and T01 count the CTA's steps (of the KV stream and
       // of each tile) before it. Without persistence they are all 0.
       auto run_item = [&](int n_t0, int n_t1, int n_steps, bool has_tail, int G0, int T00,
-                          int T01) -> bool {
+                          int T01, int item_no) -> bool {
         int s_left = n_t0 + n_t1;  // S MMA groups of this item still to issue
-        int v_ready = -1;          // last step whose V is resident (and tail-zeroed)
-        auto issue_s = [&](int t, int jj) -> bool {
+        auto issue_s = [&](int t, int jj) {
           const int gk = G0 + jj, st = gk & 1;
-          if (!wait_all(bar(kBarKFull + st), (gk >> 1) & 1)) return false;
           const uint32_t tS = tmem + t * kBN;
           const uint32_t qd = t ? q_lo1 : q_lo0;
           const uint32_t kd = st ? k_lo1 : k_lo0;
@@ -990,23 +1010,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (s_left == 0) mma_commit(bar(kBarQEmpty));
           }
           __syncwarp();
-          return true;
         };
         auto issue_pv = [&](int t, int jj) -> bool {
           const int gk = G0 + jj, st = gk & 1;
-          if (v_ready != jj) {
-            // the producer zeroes the tail of the item's last KV tile
-            bool ok;
-            if (has_tail && jj == n_steps - 1) {
-              const uint32_t par = (tail_parity >> st) & 1u;
-              tail_parity ^= 1u << st;
-              ok = wait_all(bar(kBarVTail + st), par);
-            } else {
-              ok = wait_all(bar(kBarVFull + st), (gk >> 1) & 1);
-            }
-            if (!ok) return false;
-            v_ready = jj;
-          }
           // P_t of this step is in TMEM once the softmax of tile t has arrived
           if (!wait_all(bar(kBarP + t), ((t ? T01 : T00) + jj) & 1)) return false;
           tc_fence_after();
@@ -1023,29 +1029,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           return true;
         };
-        bool ok = true;
-        if (ok && n_t0 > 0) ok = issue_s(0, 0);
-        if (ok && n_t1 > 0) ok = issue_s(1, 0);
+        // the item's first K (its own barrier, one phase per item), its first
+        // S MMAs, then release G0 (K(G0), and V(G0 - 1) of the item before)
+        bool ok = wait_all(bar(kBarK0), item_no & 1);
+        if (ok && n_t0 > 0) issue_s(0, 0);
+        if (ok && n_t1 > 0) issue_s(1, 0);
         if (ok) {
-          if (elect_one()) mma_commit(bar(kBarKEmpty + (G0 & 1)));  // K of step 0 is free once those are done
+          if (elect_one()) mma_commit(bar(kBarRel + (G0 & 1)));
           __syncwarp();
         }
         for (int jj = 1; ok && jj <= n_steps; ++jj) {
+          // V(jj - 1) and K(jj) are resident: one barrier (the producer zeroes
+          // the tail of the item's last KV tile, which comes with no K)
+          const int gb = G0 + jj - 1, sb = gb & 1;
+          if (has_tail && jj == n_steps) {
+            const uint32_t par = (tail_parity >> sb) & 1u;
+            tail_parity ^= 1u << sb;
+            ok = wait_all(bar(kBarVTail + sb), par);
+          } else {
+            ok = wait_all(bar(kBarKV + sb), (gb >> 1) & 1);
+          }
           // finish step jj-1 for every query tile, starting step jj where needed
-          if (jj - 1 < n_t0) {
+          if (ok && jj - 1 < n_t0) {
             ok = issue_pv(0, jj - 1);
-            if (ok && jj < n_t0) ok = issue_s(0, jj);
+            if (ok && jj < n_t0) issue_s(0, jj);
           }
           if (ok && jj - 1 < n_t1) {
             ok = issue_pv(1, jj - 1);
-            if (ok && jj < n_t1) ok = issue_s(1, jj);
+            if (ok && jj < n_t1) issue_s(1, jj);
           }
-          // V of step jj-1 has had its last P.V; K of step jj its last S
-          if (ok) {
-            if (elect_one()) {
-              mma_commit(bar(kBarVEmpty + ((G0 + jj - 1) & 1)));
-              if (jj < n_steps) mma_commit(bar(kBarKEmpty + ((G0 + jj) & 1)));
-            }
+          // release G0 + jj: K(G0 + jj) has had its last S, V(G0 + jj - 1)
+          // its last P.V (the item's last V is released by the next item's
+          // first release, or by the final one)
+          if (ok && jj < n_steps) {
+            if (elect_one()) mma_commit(bar(kBarRel + ((G0 + jj) & 1)));
             __syncwarp();
           }
         }
@@ -1062,12 +1079,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const volatile int *dv = reinterpret_cast<volatile int *>(smem + kItemOff);
         const int n_t0 = dv[0], n_t1 = dv[1], n_steps = dv[2], tail = dv[3];
         if (n_steps == 0) break;  // no more items
-        good = run_item(n_t0, n_t1, n_steps, tail != 0, G0, T00, T01);
+        good = run_item(n_t0, n_t1, n_steps, tail != 0, G0, T00, T01, item_no);
         G0 += n_steps;
         T00 += n_t0;
         T01 += n_t1;
       }
-      // every MMA issued here has completed before the CTA frees its TMEM
+      // the final release G0 frees the last V; every MMA issued here has
+      // completed before the CTA frees its TMEM
+      if (good && G0 > 0) {
+        if (elect_one()) mma_commit(bar(kBarRel + (G0 & 1)));
+        __syncwarp();
+      }
       if (elect_one()) mma_commit(bar(kBarDone));
       __syncwarp();
       if (!wait_all(bar(kBarDone), 0)) good = false;
