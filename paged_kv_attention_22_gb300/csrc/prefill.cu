@@ -10,12 +10,15 @@
 // queries (H_q / H_kv >= 2) the two query heads of a head pair over the same
 // 128 rows; without grouping, two consecutive row tiles of one head. 12 warps:
 //   warp 8     TMA producer: both Q tiles once, then K and V tiles of 128 keys,
-//              two stages deep, 128-byte swizzled. A tile is copied as boxes of
+//              two stages deep, 128-byte swizzled; V of step j and K of step
+//              j+1 go out together once the MMA warp's release of step j-1
+//              has freed both their stages. A tile is copied as boxes of
 //              the largest of 128, 64, 32, 16 rows that divides the block size
 //              (a box never crosses a cache block): fewer, larger copies
 //              (one 128-row box per column half streams from L2 about twice
 //              as fast per SM as eight 16-row boxes).
-//   warp 9     MMA issuer. TMEM holds S_t (128 fp32 columns) and O_t (128) for
+//   warp 9     MMAs (the whole warp runs the loop, one elected lane issues).
+//              TMEM holds S_t (128 fp32 columns) and O_t (128) for
 //              each tile t. Per KV tile j and query tile t: S_t = Q_t K_j^T
 //              (A and B from shared memory), then, once the softmax has
 //              written P_t (bf16) over the first 64 columns of S_t,
@@ -29,8 +32,9 @@
 //              per thread (TMEM lane = row). Read the S row, mask, online
 //              softmax in base 2 (the O row in TMEM is rescaled only in tiles
 //              where some row's maximum grows), write P back into TMEM; at the
-//              end normalise O and store the bf16 output and the natural-log
-//              lse.
+//              end normalise O and store the bf16 output (through a staging
+//              area per warp, so that each store writes whole row halves) and
+//              the natural-log lse.
 // While one tile's softmax runs, the tensor pipe works on the other tile.
 //
 // Two kernels share this design. Without a sliding window, prefill_kernel
@@ -83,8 +87,8 @@ constexpr int kEpiOff = (kItemOff + 32 + 127) / 128 * 128;
 constexpr int kSmemBytes = kEpiOff + 8 * kEpiWarpBytes + 1024;  // + slack for 1024-byte alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 // warps 0-7 softmax (warpgroup t for query tile t), warp 8 TMA producer,
-// warp 9 MMA issuer, warps 10-11 idle: three warpgroups, so that setmaxnreg
-// can move registers from the third to the two softmax warpgroups
+// warp 9 MMAs, warps 10-11 idle: three warpgroups, so that setmaxnreg can
+// move registers from the third to the two softmax warpgroups
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 // registers per thread after the split, 2 * softmax + other = 3 * 168 (the
@@ -743,9 +747,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Persistent: one CTA per SM walks its items. Used with a sliding window,
 // where an item is two or three KV steps and a CTA's fixed cost (a few
 // microseconds of set-up, pipeline fill and drain) would otherwise rival its
-// work. Barrier phases run on across items: K/V stages and the V-tail barriers count the CTA's KV steps, the S,
-// P and O barriers of tile t count that tile's steps, the Q barriers count
-// items. The next item's Q is loaded once every S MMA of the current item has
+// work. Barrier phases run on across items: the K/V, release and V-tail
+// barriers count the CTA's KV steps, the S, P and O barriers of tile t count
+// that tile's steps, the Q and first-K barriers count items. The next item's Q is loaded once every S MMA of the current item has
 // completed (kBarQEmpty), its first S MMAs follow the current item's last
 // P.V in issue order, and its first P.V (which overwrites O) waits for the
 // softmax warps' P, which they write only after reading the current O.
@@ -811,9 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the Q buffer), then K and V tiles of 128 keys. Lane b < kBN / box_rows
       // owns the b-th box of every KV tile: it reads that box's block-table
       // entry one tile ahead (the read overlaps the wait for a free stage) and
-      // issues the box's copies; lane 0 arms the barriers. K and V stages are
-      // released separately: K(j) once every S = Q K(j)^T is done, V(j) once
-      // every P.V(j) is.
+      // issues the box's copies; lane 0 arms the barriers.
       const int box_rows = p.box_rows;
       const int n_boxes = kBN / box_rows;
       if (lane == 0) {
