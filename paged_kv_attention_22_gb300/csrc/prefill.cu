@@ -9,7 +9,7 @@
 // One CTA owns two 128-row query tiles that share every K/V tile: with grouped
 // queries (H_q / H_kv >= 2) the two query heads of a head pair over the same
 // 128 rows; without grouping, two consecutive row tiles of one head. 12 warps:
-//   warp 8     TMA producer: both Q tiles once, then K and V tiles of 128 keys,
+//   warp 0     TMA producer: both Q tiles once, then K and V tiles of 128 keys,
 //              two stages deep, 128-byte swizzled; V of step j and K of step
 //              j+1 go out together once the MMA warp's release of step j-1
 //              has freed both their stages. A tile is copied as boxes of
@@ -17,7 +17,7 @@
 //              (a box never crosses a cache block): fewer, larger copies
 //              (one 128-row box per column half streams from L2 about twice
 //              as fast per SM as eight 16-row boxes).
-//   warp 9     MMAs (the whole warp runs the loop, one elected lane issues).
+//   warp 1     MMAs (the whole warp runs the loop, one elected lane issues).
 //              TMEM holds S_t (128 fp32 columns) and O_t (128) for
 //              each tile t. Per KV tile j and query tile t: S_t = Q_t K_j^T
 //              (A and B from shared memory), then, once the softmax has
@@ -28,7 +28,7 @@
 //              The V rows past the segment's last key are zeroed before their
 //              first P.V, so stale or poisoned rows never meet a zero
 //              probability.
-//   warps 0-3  softmax of tile 0, warps 4-7 softmax of tile 1: one query row
+//   warps 4-7  softmax of tile 0, warps 8-11 softmax of tile 1: one query row
 //              per thread (TMEM lane = row). Read the S row, mask, online
 //              softmax in base 2 (the O row in TMEM is rescaled only in tiles
 //              where some row's maximum grows), write P back into TMEM; at the
@@ -86,11 +86,15 @@ constexpr int kEpiWarpBytes = 32 * 128;
 constexpr int kEpiOff = (kItemOff + 32 + 127) / 128 * 128;
 constexpr int kSmemBytes = kEpiOff + 8 * kEpiWarpBytes + 1024;  // + slack for 1024-byte alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-// warps 0-7 softmax (warpgroup t for query tile t), warp 8 TMA producer,
-// warp 9 MMAs, warps 10-11 idle: three warpgroups, so that setmaxnreg can
-// move registers from the third to the two softmax warpgroups
+// warp 0 TMA producer, warp 1 MMAs, warps 2-3 idle, warps 4-11 softmax
+// (warpgroup 1 + t for query tile t): three warpgroups, so that setmaxnreg can
+// move registers from the first to the two softmax warpgroups. The producer
+// and MMA warps come first because the warp scheduler, choosing among ready
+// warps of one SM sub-partition, favours the lower-numbered ones: the MMA
+// warp shares its sub-partition with two busy softmax warps, and every cycle
+// it waits for an issue slot delays the tensor pipe.
 constexpr int kThreads = 384;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kProducerWarp = 0, kMmaWarp = 1, kSoftmaxWarp0 = 4;
 // registers per thread after the split, 2 * softmax + other = 3 * 168 (the
 // launch's share per thread of the 64K register file for 384 threads); the
 // same in both kernels (the persistent one's producer and MMA warp, which
@@ -372,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kTmemSlotOff);
 
-  if (warp >= kProducerWarp) {
+  if (warp < kSoftmaxWarp0) {
     setmaxnreg_dec<RegSplit<false>::kOther>();
     if (warp == kProducerWarp) {
       // ------------------------------------------------------------ TMA producer
@@ -585,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     setmaxnreg_inc<RegSplit<false>::kSoftmax>();
     // ------------------------------------------------------------ softmax / epilogue
-    const int t = warp >> 2;                // query tile of this warpgroup
+    const int t = (warp - kSoftmaxWarp0) >> 2;  // query tile of this warpgroup
     const int quad = warp & 3;              // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;         // row within the tile == TMEM lane
     const int n_t = n_tiles[t] > 0 ? n_tiles[t] - j_start : 0;  // steps of this tile
@@ -725,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = 1.f / lr;
       const bool store = qi < Lq;
       const int qw = row0[t] + quad * 32;  // query of the warp's first row
-      store_o_rows(tO, inv_l, sbase + kEpiOff + warp * kEpiWarpBytes,
+      store_o_rows(tO, inv_l, sbase + kEpiOff + (warp - kSoftmaxWarp0) * kEpiWarpBytes,
                    p.out + (static_cast<int64_t>(q0 + qw) * p.num_q_heads + head[t]) * kD,
                    static_cast<int64_t>(p.num_q_heads) * kD, min(32, Lq - qw), lane);
       if (store && p.lse != nullptr)
@@ -807,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicOr(&g_prefill_errors, kErrTimeout);
   };
 
-  if (warp >= kProducerWarp) {
+  if (warp < kSoftmaxWarp0) {
     setmaxnreg_dec<RegSplit<true>::kOther>();
     if (warp == kProducerWarp && !skipped) {
       // ------------------------------------------------------------ TMA producer
@@ -1101,7 +1105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     setmaxnreg_inc<RegSplit<true>::kSoftmax>();
     if (!skipped) {
       // ------------------------------------------------------------ softmax / epilogue
-      const int t = warp >> 2;                // query tile of this warpgroup
+      const int t = (warp - kSoftmaxWarp0) >> 2;  // query tile of this warpgroup
       const int quad = warp & 3;              // TMEM lane quadrant this warp may access
       const int r = quad * 32 + lane;         // row within the tile == TMEM lane
       const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -1273,7 +1277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float inv_l = 1.f / lr;
           const bool store = qi < Lq;
           const int qw = row0 + quad * 32;  // query of the warp's first row
-          store_o_rows(tO, inv_l, sbase + kEpiOff + warp * kEpiWarpBytes,
+          store_o_rows(tO, inv_l, sbase + kEpiOff + (warp - kSoftmaxWarp0) * kEpiWarpBytes,
                        p.out + (static_cast<int64_t>(q0 + qw) * p.num_q_heads + head_t) * kD,
                        static_cast<int64_t>(p.num_q_heads) * kD, min(32, Lq - qw), lane);
           if (store && p.lse != nullptr)
