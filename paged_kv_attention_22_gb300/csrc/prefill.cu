@@ -99,7 +99,6 @@ constexpr int kProducerWarp = 0, kMmaWarp = 1, kSoftmaxWarp0 = 4;
 // launch's share per thread of the 64K register file for 384 threads); the
 // same in both kernels (the persistent one's producer and MMA warp, which
 // reads each item from shared memory, fit in 72 without spills)
-template <bool kPersistent>
 struct RegSplit {
   static constexpr int kSoftmax = 216;
   static constexpr int kOther = 72;
@@ -377,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kTmemSlotOff);
 
   if (warp < kSoftmaxWarp0) {
-    setmaxnreg_dec<RegSplit<false>::kOther>();
+    setmaxnreg_dec<RegSplit::kOther>();
     if (warp == kProducerWarp) {
       // ------------------------------------------------------------ TMA producer
       // Lane b < kBN / box_rows owns the b-th box of every KV tile: it reads
@@ -587,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!good && lane == 0) fail(abort);
     }
   } else {
-    setmaxnreg_inc<RegSplit<false>::kSoftmax>();
+    setmaxnreg_inc<RegSplit::kSoftmax>();
     // ------------------------------------------------------------ softmax / epilogue
     const int t = (warp - kSoftmaxWarp0) >> 2;  // query tile of this warpgroup
     const int quad = warp & 3;              // TMEM lane quadrant this warp may access
@@ -812,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp < kSoftmaxWarp0) {
-    setmaxnreg_dec<RegSplit<true>::kOther>();
+    setmaxnreg_dec<RegSplit::kOther>();
     if (warp == kProducerWarp && !skipped) {
       // ------------------------------------------------------------ TMA producer
       // Per item: both Q tiles (once the previous item's S MMAs are done with
@@ -1102,7 +1101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!good && lane == 0) fail();
     }
   } else {
-    setmaxnreg_inc<RegSplit<true>::kSoftmax>();
+    setmaxnreg_inc<RegSplit::kSoftmax>();
     if (!skipped) {
       // ------------------------------------------------------------ softmax / epilogue
       const int t = (warp - kSoftmaxWarp0) >> 2;  // query tile of this warpgroup
