@@ -1335,7 +1335,7 @@ cudaError_t launch_instance(dim3 grid, const CUtensorMap &q_map, const CUtensorM
                ? fa.numRegs
                : 0;
   }();
-  using R = RegSplit<kPersistent>;
+  using R = RegSplit;
   if (launch_regs * kThreads < (2 * R::kSoftmax + R::kOther) * 128)
     return cudaErrorInvalidConfiguration;
   return launch_pdl(kern, grid, dim3(kThreads), kSmemBytes, stream, q_map, k_map, v_map, p);
