@@ -139,6 +139,22 @@ def test_windowed_prefill_one_query_head_per_kv_head():
         _check_prefill(case, window)
 
 
+def test_windowed_prefill_four_query_heads_per_kv_head():
+    # a KV head serving four query heads: an item holds two of them, and the
+    # other two of the same KV head form another item over the same rows
+    case = W.prefill_case("pwin-g4", 37, [300, 7, 130], [420, 7, 130], block_size=64,
+                          num_blocks=24, blocks_per_seq=8, H_q=32, H_kv=8)
+    for window in (1, 64, 200):
+        _check_prefill(case, window)
+
+
+def test_windowed_decode_four_query_heads_per_kv_head():
+    case = W.decode_case("dwin-g4", 38, [77, 300, 1, 160], block_size=32, num_blocks=40,
+                         blocks_per_seq=10, H_q=32, H_kv=8)
+    for window in (1, 40, 200):
+        _check_decode(case, window, what="4 query heads per KV head")
+
+
 def test_windowed_prefix8k_prefill_full():
     # the full-size prefix workload with the SWA-256 window: every output
     # element and every lse against the windowed fp64 oracle
