@@ -712,6 +712,9 @@ def main(argv=None):
                     help="layers per step (28 for the real workload; fewer for profiling)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the sliding-window, head-shard and block-manager legs")
+    ap.add_argument("--prefill-window", type=int, default=0,
+                    help="sliding window of the prefill leg (0: none; the windowed kernel "
+                         "alone, for profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -804,17 +807,22 @@ def main(argv=None):
 
     prefill = None
     if not args.no_prefill:
-        pr = time_prefill(pkv, min(args.steps, 20), args.warmup)
+        pr = time_prefill(pkv, min(args.steps, 20), args.warmup, window=args.prefill_window)
         tflops = pr["flops"] / (pr["prefill_ms"] / 1000.0) / 1e12
-        store_gbs = pr["store_bytes"] / (pr["store_ms"] / 1000.0) / 1e9
+        # the store is timed with the unwindowed leg only
+        store_gbs = (pr["store_bytes"] / (pr["store_ms"] / 1000.0) / 1e9
+                     if pr["store_ms"] is not None else None)
+        window_note = (f", sliding window {args.prefill_window}" if args.prefill_window > 0
+                       else "")
         prefill = {"workload": "prefix-cached prefill: 8 seqs x 4096 new tokens over a shared "
-                               "4096-token cached prefix (Lk 8192), bs=256",
+                               "4096-token cached prefix (Lk 8192), bs=256" + window_note,
                    "value": tflops, "unit": "TFLOP/s", "ms_per_call": pr["prefill_ms"],
                    "flops_per_call": pr["flops"],
                    "frac": tflops / peaks["bf16_tflops"], "peak": peaks["bf16_tflops"],
                    "peak_kind": f"bf16 dense burst ({peaks['source']})",
                    "kv_store_gbs": store_gbs,
-                   "kv_store_frac": store_gbs / peaks["hbm_gbs"],
+                   "kv_store_frac": (store_gbs / peaks["hbm_gbs"]
+                                     if store_gbs is not None else None),
                    "timing": "20 calls back to back between two CUDA events, per call",
                    "kv_store_tokens": 32768,
                    "kv_store_timing": "slope between 8 and 24 back-to-back stores rotating over "
